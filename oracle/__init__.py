@@ -1,0 +1,147 @@
+"""Plain, slow CPU oracle for the TwoTower denoising-step hot path.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only code allowed to import this package.
+It shares no code with the CUDA path (no kernels, headers, helpers, tables or
+constant generators); the two meet only in the seeded input generator
+``block_diffusion_decoding_attn_b300.workload``, which holds none of the
+method's arithmetic.
+
+* ``block_attn`` follows "Nemotron-Labs-TwoTower" Section 2.1, Eq. (1): one
+  softmax per query over [context keys; block keys], fp64, explicit loops
+  (``attn_ref.c``).
+* ``commit`` follows Section 2.2 / Algorithm 2 (confidence unmasking) with a
+  fixed per-step budget k and the canonical fixed-point confidence key
+  (``commit_ref.c``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "liboracle.so")
+_SRC = [os.path.join(_HERE, "attn_ref.c"), os.path.join(_HERE, "commit_ref.c")]
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (no fp contraction: fmaf is called explicitly)."""
+    newest = max(os.path.getmtime(s) for s in _SRC)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < newest:
+        tmp = _SO + f".{os.getpid()}.tmp"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+               "-ffp-contract=off", "-fno-fast-math", "-o", tmp] + _SRC + ["-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            lib.tt_oracle_block_attn.restype = ctypes.c_int
+            lib.tt_oracle_block_attn.argtypes = [ctypes.c_int] * 6 + [ctypes.c_double] + [P] * 6 + [
+                ctypes.c_int, P, P, ctypes.c_int]
+            lib.tt_oracle_exp_own.restype = ctypes.c_float
+            lib.tt_oracle_exp_own.argtypes = [ctypes.c_float]
+            lib.tt_oracle_quant.restype = ctypes.c_uint64
+            lib.tt_oracle_quant.argtypes = [ctypes.c_float]
+            lib.tt_oracle_row_key.restype = None
+            lib.tt_oracle_row_key.argtypes = [P, ctypes.c_long, P, P]
+            lib.tt_oracle_commit.restype = ctypes.c_int
+            lib.tt_oracle_commit.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_long, P,
+                                             ctypes.c_int, P, P, P, P, ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, scale=None, rows=None, threads=0):
+    """fp64 block attention (Eq. 1).
+
+    q [B][L][Hq][D], k_blk/v_blk [B][L][Hkv][D], k_ctx/v_ctx [B][Hkv][C_cap][D]
+    as bf16 bit patterns (uint16); ctx_len [B] int32. ``scale`` None means
+    1/sqrt(D). ``rows`` None gives the full [B][L][Hq][D] output; otherwise an
+    [n][3] int array of (b, l, h) triples and an [n][D] output.
+    """
+    lib = _load()
+    q, k_blk, v_blk = _c(q, np.uint16), _c(k_blk, np.uint16), _c(v_blk, np.uint16)
+    k_ctx, v_ctx = _c(k_ctx, np.uint16), _c(v_ctx, np.uint16)
+    ctx_len = _c(ctx_len, np.int32)
+    B, L, Hq, D = q.shape
+    Hkv, C = k_ctx.shape[1], k_ctx.shape[2]
+    assert k_blk.shape == (B, L, Hkv, D) and v_blk.shape == k_blk.shape
+    assert k_ctx.shape == (B, Hkv, C, D) and v_ctx.shape == k_ctx.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    if rows is None:
+        out = np.empty((B, L, Hq, D), np.float64)
+        n, rp = 0, None
+    else:
+        rows = _c(rows, np.int32).reshape(-1, 3)
+        out = np.empty((rows.shape[0], D), np.float64)
+        n, rp = rows.shape[0], _ptr(rows)
+    rc = lib.tt_oracle_block_attn(B, L, Hq, Hkv, D, C, float(scale), _ptr(q), _ptr(k_blk),
+                                  _ptr(v_blk), _ptr(k_ctx), _ptr(v_ctx), _ptr(ctx_len), n, rp,
+                                  _ptr(out), int(threads))
+    if rc != 0:
+        raise ValueError("oracle block_attn: invalid arguments")
+    return out
+
+
+def exp_own(x: float) -> float:
+    """The fp32 exponential that defines the canonical confidence key."""
+    return _load().tt_oracle_exp_own(float(np.float32(x)))
+
+
+def quant(x: float) -> int:
+    """q(x) = rint(2^40 * e(x)) as an integer (0 below -30)."""
+    return int(_load().tt_oracle_quant(float(np.float32(x))))
+
+
+def row_key(row) -> tuple[int, int]:
+    """(greedy prediction, canonical key) of one fp32 logit row."""
+    lib = _load()
+    row = _c(row, np.float32)
+    a = np.zeros(1, np.int32)
+    k = np.zeros(1, np.uint64)
+    lib.tt_oracle_row_key(_ptr(row), row.shape[0], _ptr(a), _ptr(k))
+    return int(a[0]), int(k[0])
+
+
+def commit(logits, B, L, masked, k, tok, threads=0):
+    """One confidence-unmasking step with budget k per block.
+
+    Returns (tok_out, masked_out, keys, args); keys/args hold the key and
+    prediction of each row that was masked on entry (0 elsewhere).
+    """
+    lib = _load()
+    logits = _c(logits, np.float32)
+    R, V = logits.shape
+    assert R == B * L
+    m_in = _c(masked, np.uint8).copy()
+    tok_out = _c(tok, np.int32).copy()
+    m_out = np.empty(R, np.uint8)
+    keys = np.zeros(R, np.uint64)
+    args = np.zeros(R, np.int32)
+    rc = lib.tt_oracle_commit(_ptr(logits), B, L, V, _ptr(m_in), int(k), _ptr(tok_out),
+                              _ptr(m_out), _ptr(keys), _ptr(args), int(threads))
+    if rc != 0:
+        raise ValueError("oracle commit: invalid arguments")
+    return tok_out, m_out, keys, args

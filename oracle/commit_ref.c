@@ -1,0 +1,148 @@
+/*
+ * CPU oracle for the unmask/commit step -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load this code. It shares nothing with the CUDA path.
+ *
+ * Method followed: "Nemotron-Labs-TwoTower" Section 2.2, "Sampling", and
+ * Algorithm 2 (single-block confidence unmasking): at each step the denoiser
+ * predicts every still-masked position in parallel, the confident predictions
+ * are committed, and the rest stay masked. ConfidenceSample is not spelled out
+ * on the page; the reading used here (a fixed budget of k commits per block per
+ * step) is Algorithm 2 with a threshold above 1 and T = L/k steps.
+ *
+ * Per still-masked row r (a scalar loop, in the order below):
+ *   1. m = max_v l[r][v]; a = lowest v with l[r][v] == m (greedy prediction).
+ *   2. confidence = max softmax probability = 1 / sum_v exp(l[r][v] - m),
+ *      computed as the canonical fixed-point key
+ *          key = sum_v q(RN32(l[r][v] - m)),   q(x) = rint(2^40 * e(x))
+ *      with e the fp32 exponential defined in own_exp below; the integer sum
+ *      does not depend on summation order. Smaller key = more confident.
+ *   3. Per block: sort the masked rows by (key ascending, row ascending) and
+ *      commit the first min(k, #masked): tok[r] = a, masked[r] = 0.
+ *
+ * The exponential (a reading: the page only says "confidence"):
+ *   x < -30          -> q = 0  (2^40 * exp(-30) < 0.11 rounds to 0 anyway)
+ *   t = RN32(x * LOG2E), n = round-half-even(t)
+ *   r = fma(-n, C1, x); r = fma(-n, C2, r)      (Cody and Waite reduction)
+ *   p = c7; p = fma(p, r, c_j) for j = 6..0     (Taylor series, c_j = 1/j!)
+ *   q = round-half-even(p * 2^(n+40))           (exact power-of-two scale)
+ * with LOG2E = RN32(1/ln 2), C1 = RN32(ln 2), C2 = RN32(ln 2 - C1),
+ * c_j = RN32(1/j!). fmaf is the correctly rounded fused multiply-add.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define LN2_D 0.69314718055994530942
+static const float LOG2E_F = (float)(1.0 / LN2_D);
+static const float C1_F = (float)LN2_D;
+
+static float c2_f(void) { return (float)(LN2_D - (double)C1_F); }
+
+/* e(x) for -30 <= x <= 0 as a float: p(r) * 2^n. Returns 0 below -30. */
+float tt_oracle_exp_own(float x) {
+    if (x < -30.0f) return 0.0f;
+    const float t = x * LOG2E_F;
+    const float n = rintf(t); /* default rounding mode: to nearest, ties to even */
+    float r = fmaf(-n, C1_F, x);
+    r = fmaf(-n, c2_f(), r);
+    static const double inv_fact[8] = {1.0, 1.0, 1.0 / 2, 1.0 / 6, 1.0 / 24, 1.0 / 120, 1.0 / 720,
+                                       1.0 / 5040};
+    float p = (float)inv_fact[7];
+    for (int j = 6; j >= 0; --j) p = fmaf(p, r, (float)inv_fact[j]);
+    return ldexpf(p, (int)n);
+}
+
+/* q(x) = rint(2^40 * e(x)). */
+uint64_t tt_oracle_quant(float x) {
+    if (x < -30.0f) return 0;
+    const float t = x * LOG2E_F;
+    const float n = rintf(t);
+    float r = fmaf(-n, C1_F, x);
+    r = fmaf(-n, c2_f(), r);
+    static const double inv_fact[8] = {1.0, 1.0, 1.0 / 2, 1.0 / 6, 1.0 / 24, 1.0 / 120, 1.0 / 720,
+                                       1.0 / 5040};
+    float p = (float)inv_fact[7];
+    for (int j = 6; j >= 0; --j) p = fmaf(p, r, (float)inv_fact[j]);
+    const float y = ldexpf(p, (int)n + 40); /* exact: a power-of-two scale of a normal */
+    return (uint64_t)rintf(y);
+}
+
+/* Greedy prediction and canonical confidence key of one row. */
+void tt_oracle_row_key(const float* row, long V, int32_t* arg, uint64_t* key) {
+    float m = row[0];
+    long a = 0;
+    for (long v = 1; v < V; ++v)
+        if (row[v] > m) { m = row[v]; a = v; } /* strict: first occurrence wins */
+    uint64_t s = 0;
+    for (long v = 0; v < V; ++v) {
+        const float x = row[v] - m; /* one fp32 subtraction, round to nearest */
+        s += tt_oracle_quant(x);
+    }
+    *arg = (int32_t)a;
+    *key = s;
+}
+
+typedef struct { uint64_t key; int32_t row; } keyed_row;
+
+static int cmp_keyed(const void* pa, const void* pb) {
+    const keyed_row* a = (const keyed_row*)pa;
+    const keyed_row* b = (const keyed_row*)pb;
+    if (a->key != b->key) return a->key < b->key ? -1 : 1;
+    return (a->row > b->row) - (a->row < b->row);
+}
+
+/*
+ * One commit step over B blocks of L rows. tok is updated in place at the
+ * committed rows only; masked_out receives the new mask (may equal masked).
+ * keys_out / args_out (may be NULL) receive the key and prediction of every
+ * masked row (untouched for unmasked rows). Returns 0, or -1 on bad arguments.
+ */
+int tt_oracle_commit(const float* logits, int B, int L, long V, const uint8_t* masked, int k,
+                     int32_t* tok, uint8_t* masked_out, uint64_t* keys_out,
+                     int32_t* args_out, int nthreads) {
+    if (B < 0 || L < 0 || V < 1 || k < 1) return -1;
+    const long R = (long)B * L;
+    uint64_t* key = (uint64_t*)malloc(sizeof(uint64_t) * (R ? R : 1));
+    int32_t* arg = (int32_t*)malloc(sizeof(int32_t) * (R ? R : 1));
+    uint8_t* m_in = (uint8_t*)malloc(R ? R : 1);
+    keyed_row* buf = (keyed_row*)malloc(sizeof(keyed_row) * (L ? L : 1));
+    if (!key || !arg || !m_in || !buf) { free(key); free(arg); free(m_in); free(buf); return -1; }
+    memcpy(m_in, masked, R);
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long r = 0; r < R; ++r)
+        if (m_in[r]) tt_oracle_row_key(logits + (size_t)r * V, V, &arg[r], &key[r]);
+
+    for (int b = 0; b < B; ++b) {
+        int n = 0;
+        for (int i = 0; i < L; ++i) {
+            const long r = (long)b * L + i;
+            if (m_in[r]) { buf[n].key = key[r]; buf[n].row = i; ++n; }
+        }
+        qsort(buf, n, sizeof(keyed_row), cmp_keyed);
+        for (int i = 0; i < L; ++i) masked_out[(long)b * L + i] = m_in[(long)b * L + i];
+        const int c = n < k ? n : k;
+        for (int j = 0; j < c; ++j) {
+            const long r = (long)b * L + buf[j].row;
+            tok[r] = arg[r];
+            masked_out[r] = 0;
+        }
+    }
+    for (long r = 0; r < R; ++r)
+        if (m_in[r]) {
+            if (keys_out) keys_out[r] = key[r];
+            if (args_out) args_out[r] = arg[r];
+        }
+    free(key); free(arg); free(m_in); free(buf);
+    return 0;
+}
