@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Benchmark of one TwoTower denoising step on B300: block attention + commit.
+
+A step is one pass of the whole hot path over one batch: tt_block_attn (one
+denoiser layer's block attention over the context KV cache, "Nemotron-Labs-
+TwoTower" Section 2.1 Eq. 1) followed by tt_commit (one confidence-unmasking
+step, Section 2.2 Algorithm 2, k commits per block) on a fully masked block.
+
+Metric: denoised block-tokens per second per layer-step (B*L tokens per step),
+plus each call's fraction of its roofline (tensor TFLOP/s for attention, HBM
+GB/s for commit) against MEASURED_PEAKS.json.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Under torchrun (N > 1) every rank runs its own batch on its own GPU (weak
+scaling, no data-path collective); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from block_diffusion_decoding_attn_b300 import workload as wl  # noqa: E402
+
+DEFAULT_WORKLOAD = "b8_c4096_l32"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def attn_flops(w, ctx):
+    return 4.0 * w.Hq * w.D * w.L * float(np.sum(ctx.astype(np.int64) + w.L))
+
+
+def attn_bytes(w, ctx):
+    kv = 2.0 * 2 * w.Hkv * w.D * float(np.sum(ctx.astype(np.int64)))
+    return kv + 2.0 * w.B * w.L * w.Hq * w.D * 2 + 2.0 * 2 * w.B * w.L * w.Hkv * w.D
+
+
+def commit_bytes(w, masked_rows):
+    committed = min(w.k, w.L) * w.B
+    return float(masked_rows) * w.V * 4 + w.rows * 2 + committed * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+def file_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(kernel, {}).get(workload)
+    if not e:
+        return None
+    src = os.path.join(ROOT, e["source"])
+    if not os.path.exists(src) or file_hash(src) != e["source_sha256"]:
+        return None  # the kernel changed since the counters were taken
+    return e["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """Polls SM clock and throttle reasons through NVML while the timed region runs."""
+
+    REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
+        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
+        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+    }
+
+    def __init__(self, index, period=0.005):
+        self.index, self.period = index, period
+        self.samples, self.reasons = [], set()
+        self._stop = threading.Event()
+        self._t = None
+        self.max_mhz = None
+        self.ok = False
+
+    def __enter__(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        except Exception:
+            self.ok = False
+        return self
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for name, bit in self.REASONS.items():
+                    if r & bit and name != "gpu_idle":
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": len(self.samples)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+def config_of(w, ctx):
+    c = {"workload": w.name, "B": w.B, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+         "ctx_len": (int(ctx[0]) if len(set(ctx.tolist())) == 1
+                     else f"{int(ctx.min())}..{int(ctx.max())} ragged, sum {int(ctx.sum())}"),
+         "ctx_cap": w.ctx_cap, "V": w.V, "k": w.k, "layer_calls_per_step": 1,
+         "commit_state": "fully masked block (first denoising step)",
+         "l2": "flushed between steps (256 MiB write, outside the timed events)"}
+    return c
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+def cpu_oracle_step(w, inp, cinp, seqs, threads=0):
+    """The oracle on whole sequences `seqs`: attention rows + commit of their blocks."""
+    import oracle
+    rows = np.array([[b, l, h] for b in seqs for l in range(w.L) for h in range(w.Hq)], np.int32)
+    oracle.block_attn(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx, inp.v_ctx, inp.ctx_len,
+                      rows=rows, threads=threads)
+    for b in seqs:
+        sl = slice(b * w.L, (b + 1) * w.L)
+        oracle.commit(cinp.logits[sl], 1, w.L, cinp.masked[sl], w.k, cinp.tok[sl],
+                      threads=threads)
+    return len(seqs) * w.L
+
+
+def cpu_baseline(w, inp, cinp, budget_s=12.0):
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    done = cpu_oracle_step(w, inp, cinp, [0])
+    t1 = time.perf_counter()
+    per_seq = t1 - t0
+    n = max(1, min(w.B - 1, int(budget_s / max(per_seq, 1e-6)) - 1))
+    seqs = list(range(1, 1 + n))
+    t2 = time.perf_counter()
+    done = cpu_oracle_step(w, inp, cinp, seqs)
+    dt = time.perf_counter() - t2
+    return {"value": done / dt, "unit": "block-tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.B} sequences ({done} block tokens, all {w.Hq} heads, "
+                      f"attention fp64 loops + scalar commit), {dt:.2f} s"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = wl.attn_inputs(w, seed=0)
+    cinp = wl.commit_inputs(w, seed=0)
+    cores = os.cpu_count() or 1
+    # each step: one whole sequence (cycling), so K steps stay within minutes
+    for i in range(args.warmup):
+        cpu_oracle_step(w, inp, cinp, [i % w.B])
+    t0 = time.perf_counter()
+    tokens = 0
+    for i in range(args.steps):
+        tokens += cpu_oracle_step(w, inp, cinp, [i % w.B])
+    dt = time.perf_counter() - t0
+    v = tokens / dt
+    line = {"metric": "denoised block-tokens/s per layer-step", "value": v,
+            "unit": "block-tokens/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Philox normals)", "config": config_of(w, inp.ctx_len),
+            "cpu_baseline": {"value": v, "unit": "block-tokens/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"one sequence per step ({w.L} block tokens, all heads)"},
+            "e2e": {"value": v, "unit": "block-tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, w):
+    import torch
+    import block_diffusion_decoding_attn_b300 as tt
+    from block_diffusion_decoding_attn_b300 import build
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if dist:
+        dist.barrier()
+    h = tt.handle(local)
+
+    # inputs resident in HBM before timing (each rank its own batch)
+    inp = wl.attn_inputs(w, seed=rank)
+    cinp = wl.commit_inputs(w, seed=rank)
+    A = wl.attn_tensors(inp, dev, pin=True)
+    Cm = wl.commit_tensors(cinp, dev, pin=True)
+    out = torch.empty_like(A["q"])
+    m_out = torch.empty_like(Cm["masked"])
+    desc = tt.attn_desc(A["q"], A["k_ctx"])
+    ws_a_n = tt.block_attn_workspace_bytes(desc, h)
+    ws_a = torch.empty(max(ws_a_n, 256), dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(max(tt.commit_workspace_bytes(w.B, w.L), 256), dtype=torch.uint8,
+                       device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 1 + (1 if ws_a_n > 0 else 0) + 2
+
+    def step():
+        tt.block_attn(A["q"], A["k_blk"], A["v_blk"], A["k_ctx"], A["v_ctx"], A["ctx_len"],
+                      out=out, workspace=ws_a, h=h, stream=stream)
+        tt.commit(Cm["logits"], w.B, w.L, Cm["masked"], w.k, Cm["tok"], masked_out=m_out,
+                  workspace=ws_c, h=h, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if h.get_error():
+        raise RuntimeError("device status set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with ClockSampler(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            tt.block_attn(A["q"], A["k_blk"], A["v_blk"], A["k_ctx"], A["v_ctx"], A["ctx_len"],
+                          out=out, workspace=ws_a, h=h, stream=stream)
+            e1.record(stream)
+            tt.commit(Cm["logits"], w.B, w.L, Cm["masked"], w.k, Cm["tok"], masked_out=m_out,
+                      workspace=ws_c, h=h, stream=stream)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        if dist:
+            dist.barrier()
+    st = h.get_error()
+    if st:
+        raise RuntimeError(f"device status {st} during the timed region")
+    t_attn = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    t_comm = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    ms_step = (sum(t_attn) + sum(t_comm)) / K
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tokens = w.B * w.L * world
+    value = tokens / (ms_step * 1e-3)
+
+    # end to end through the public API: host (pinned) buffers in, results out
+    host_in = {k: v.cpu().pin_memory() for k, v in list(A.items()) + list(Cm.items())}
+    host_out = {"out": torch.empty_like(out, device="cpu").pin_memory(),
+                "tok": torch.empty_like(Cm["tok"], device="cpu").pin_memory(),
+                "masked": torch.empty_like(m_out, device="cpu").pin_memory()}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    Ke = max(3, min(K, 20))
+
+    def e2e_step():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        tt.block_attn(dev_in["q"], dev_in["k_blk"], dev_in["v_blk"], dev_in["k_ctx"],
+                      dev_in["v_ctx"], dev_in["ctx_len"], out=out, workspace=ws_a, h=h,
+                      stream=stream)
+        tt.commit(dev_in["logits"], w.B, w.L, dev_in["masked"], w.k, dev_in["tok"],
+                  masked_out=m_out, workspace=ws_c, h=h, stream=stream)
+        host_out["out"].copy_(out, non_blocking=True)
+        host_out["tok"].copy_(dev_in["tok"], non_blocking=True)
+        host_out["masked"].copy_(m_out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    te0 = time.perf_counter()
+    for _ in range(Ke):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - te0) / Ke * 1e3
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        dist.destroy_process_group() if dist else None
+        return 0
+
+    peaks = load_peaks()
+    a_ms, c_ms = statistics.mean(t_attn), statistics.mean(t_comm)
+    fl, by_a = attn_flops(w, inp.ctx_len), attn_bytes(w, inp.ctx_len)
+    by_c = commit_bytes(w, int(cinp.masked.sum()))
+    attn_tf = fl / (a_ms * 1e-3) / 1e12
+    comm_gbs = by_c / (c_ms * 1e-3) / 1e9
+    roof_attn = {"bound": "tensor", "achieved": attn_tf, "peak": peaks["bf16_tflops"],
+                 "unit": "TFLOP/s", "frac": attn_tf / peaks["bf16_tflops"],
+                 "traffic": profiled_traffic("block_attn", w.name),
+                 "kernel": "tt_block_attn call (attention kernel + split merge)",
+                 "algorithmic": f"{fl:.4g} FLOP, {by_a:.4g} B per call",
+                 "ms": a_ms, "peak_source": peaks["source"] + " burst"}
+    roof_comm = {"bound": "hbm", "achieved": comm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": comm_gbs / peaks["hbm_gbs"],
+                 "traffic": profiled_traffic("commit", w.name),
+                 "kernel": "tt_commit call (row reduction + top-k select)",
+                 "algorithmic": f"{by_c:.4g} B per call", "ms": c_ms,
+                 "peak_source": peaks["source"]}
+    dom = roof_attn if a_ms >= c_ms else roof_comm
+    line = {
+        "metric": "denoised block-tokens/s per layer-step", "value": value,
+        "unit": "block-tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (attention, fp32 accumulate) / f32 (commit)",
+        "data": "synthetic (seeded Philox normals; inputs resident in HBM)",
+        "config": config_of(w, inp.ctx_len),
+        "roofline": dom,
+        "kernels": {"attention": roof_attn, "commit": roof_comm},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "block-tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "steps": Ke},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, cinp)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = wl.WORKLOADS[args.workload]
+    if w.ctx_schedule:
+        raise SystemExit("multi-call schedules are parity cases; bench a single-call workload")
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,227 @@
+"""TwoTower denoising-step hot path on B300 (sm_103a): block attention and
+unmask/commit, as hand-written CUDA kernels behind the C ABI in ``include/tt.h``.
+
+This module is argument marshalling only: it turns torch tensors (device
+memory, streams) into the plain pointers and sizes of the C ABI and calls
+``libtt.so``. Every step of the computation runs in the library's kernels.
+There is no CPU fallback: without the built library or a CUDA device every
+entry point raises.
+
+Entry points mirror the C ABI:
+
+* :func:`block_attn` -> ``tt_block_attn`` ("Nemotron-Labs-TwoTower",
+  Section 2.1, Eq. 1)
+* :func:`commit` -> ``tt_commit`` (Section 2.2, Algorithm 2 with k commits per
+  block per step)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtt.so")
+
+TT_OK = 0
+TT_DEV_CTX_LEN_RANGE = 1
+TT_DEV_WAIT_TIMEOUT = 2
+
+_lock = threading.Lock()
+_lib = None
+_handles: dict[int, "Handle"] = {}
+
+
+class TTError(RuntimeError):
+    """A C-ABI call returned an error status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libtt.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: run block_diffusion_decoding_attn_b300."
+                                  "build.build() (nvcc, sm_103a) first")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.tt_create.argtypes = [ctypes.POINTER(P), I]
+            L.tt_destroy.argtypes = [P]
+            L.tt_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+            L.tt_set_wait_timeout.argtypes = [P, ctypes.c_ulonglong]
+            L.tt_status_string.restype = ctypes.c_char_p
+            L.tt_status_string.argtypes = [I]
+            L.tt_last_error.restype = ctypes.c_char_p
+            L.tt_last_error.argtypes = []
+            L.tt_block_attn_workspace_bytes.restype = S
+            L.tt_block_attn_workspace_bytes.argtypes = [P, ctypes.POINTER(AttnDesc)]
+            L.tt_block_attn.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 7 + [P, S, P]
+            L.tt_commit_workspace_bytes.restype = S
+            L.tt_commit_workspace_bytes.argtypes = [I, I]
+            L.tt_commit.argtypes = [P, P, I, I, I, P, I, P, P, P, S, P]
+            for f in ("tt_create", "tt_destroy", "tt_get_error", "tt_set_wait_timeout",
+                      "tt_block_attn", "tt_commit"):
+                getattr(L, f).restype = I
+            _lib = L
+    return _lib
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("Hq", ctypes.c_int),
+                ("Hkv", ctypes.c_int), ("D", ctypes.c_int), ("ctx_cap", ctypes.c_int),
+                ("scale", ctypes.c_float), ("num_splits", ctypes.c_int)]
+
+
+def _check(status: int, what: str):
+    if status != TT_OK:
+        L = lib()
+        msg = L.tt_last_error().decode() or L.tt_status_string(status).decode()
+        raise TTError(status, f"{what}: {msg}")
+
+
+class Handle:
+    """A library handle bound to one CUDA device (``tt_create``)."""
+
+    def __init__(self, device: int = 0):
+        self.device = device
+        self._h = ctypes.c_void_p()
+        _check(lib().tt_create(ctypes.byref(self._h), device), "tt_create")
+
+    @property
+    def ptr(self):
+        return self._h
+
+    def get_error(self) -> int:
+        """Synchronizes the device; returns and clears the TT_DEV_* status bits."""
+        st = ctypes.c_uint(0)
+        rc = lib().tt_get_error(self._h, ctypes.byref(st))
+        if rc not in (TT_OK, -4):
+            _check(rc, "tt_get_error")
+        return st.value
+
+    def set_wait_timeout(self, ns: int):
+        _check(lib().tt_set_wait_timeout(self._h, int(ns)), "tt_set_wait_timeout")
+
+    def close(self):
+        if self._h:
+            lib().tt_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def handle(device: int | None = None) -> Handle:
+    """The process-wide handle of `device` (default: torch's current device)."""
+    import torch
+    if device is None:
+        device = torch.cuda.current_device()
+    with _lock:
+        h = _handles.get(device)
+    if h is None:
+        h = Handle(device)
+        with _lock:
+            _handles.setdefault(device, h)
+            h = _handles[device]
+    return h
+
+
+def _stream_ptr(t, stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev_ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def attn_desc(q, k_ctx, scale: float = 0.0, num_splits: int = 0) -> AttnDesc:
+    B, L, Hq, D = q.shape
+    Hkv, C = k_ctx.shape[1], k_ctx.shape[2]
+    return AttnDesc(B, L, Hq, Hkv, D, C, float(scale), int(num_splits))
+
+
+def block_attn_workspace_bytes(desc: AttnDesc, h: Handle | None = None) -> int:
+    h = h or handle()
+    return int(lib().tt_block_attn_workspace_bytes(h.ptr, ctypes.byref(desc)))
+
+
+def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out=None, scale: float = 0.0,
+               num_splits: int = 0, workspace=None, h: Handle | None = None, stream=None):
+    """Block attention, Eq. (1): one softmax per query over [context keys; block keys].
+
+    q [B][L][Hq][D], k_blk/v_blk [B][L][Hkv][D], k_ctx/v_ctx [B][Hkv][C_cap][D]
+    (torch.bfloat16, CUDA, contiguous); ctx_len [B] int32 on the device.
+    Returns out [B][L][Hq][D] bf16.
+    """
+    import torch
+    for name, t in (("q", q), ("k_blk", k_blk), ("v_blk", v_blk), ("k_ctx", k_ctx),
+                    ("v_ctx", v_ctx)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    if ctx_len.dtype != torch.int32 or not ctx_len.is_cuda:
+        raise ValueError("ctx_len must be an int32 CUDA tensor")
+    h = h or handle(q.device.index)
+    desc = attn_desc(q, k_ctx, scale, num_splits)
+    if out is None:
+        out = torch.empty_like(q)
+    need = block_attn_workspace_bytes(desc, h)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wsp = _dev_ptr(workspace) if need else ctypes.c_void_p(0)
+    wsn = workspace.numel() * workspace.element_size() if need else 0
+    _check(lib().tt_block_attn(h.ptr, ctypes.byref(desc), _dev_ptr(q), _dev_ptr(k_blk),
+                               _dev_ptr(v_blk), _dev_ptr(k_ctx), _dev_ptr(v_ctx),
+                               _dev_ptr(ctx_len), _dev_ptr(out), wsp, wsn,
+                               _stream_ptr(q, stream)), "tt_block_attn")
+    return out
+
+
+def commit_workspace_bytes(B: int, L: int) -> int:
+    return int(lib().tt_commit_workspace_bytes(int(B), int(L)))
+
+
+def commit(logits, B: int, L: int, masked, k: int, tok, masked_out=None, workspace=None,
+           h: Handle | None = None, stream=None):
+    """One unmask/commit step (Algorithm 2, budget k per block).
+
+    logits [B*L][V] float32, masked [B*L] uint8, tok [B*L] int32 (updated in
+    place at committed rows). Returns (tok, masked_out, workspace); the
+    workspace holds key[B*L] (uint64) then arg[B*L] (int32).
+    """
+    import torch
+    if logits.dtype != torch.float32 or not logits.is_cuda or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous CUDA float32 tensor")
+    if masked.dtype != torch.uint8 or tok.dtype != torch.int32:
+        raise ValueError("masked must be uint8 and tok int32")
+    h = h or handle(logits.device.index)
+    if masked_out is None:
+        masked_out = torch.empty_like(masked)
+    need = commit_workspace_bytes(B, L)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=logits.device)
+    _check(lib().tt_commit(h.ptr, _dev_ptr(logits), int(B), int(L), int(logits.shape[1]),
+                           _dev_ptr(masked), int(k), _dev_ptr(tok), _dev_ptr(masked_out),
+                           _dev_ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream_ptr(logits, stream)), "tt_commit")
+    return tok, masked_out, workspace
+
+
+def commit_keys(workspace, B: int, L: int):
+    """Views of (key[B*L] as int64 bits, arg[B*L]) inside a commit workspace."""
+    import torch
+    rows = B * L
+    off = (rows * 8 + 255) // 256 * 256
+    keys = workspace[:rows * 8].view(torch.int64)
+    args = workspace[off:off + rows * 4].view(torch.int32)
+    return keys, args

@@ -1,0 +1,63 @@
+// Internal interface between the C-ABI layer (tt_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace tt {
+
+// Device status bits (accumulated in the handle's status word).
+constexpr unsigned kDevCtxLenRange = 1u;  // ctx_len[b] outside [0, ctx_cap]; clamped
+constexpr unsigned kDevWaitTimeout = 2u;  // a bounded pipeline wait gave up
+
+constexpr int kTile = 128;  // query rows per M tile and keys per KV tile
+
+struct AttnParams {
+    int B, L, Hq, Hkv, G, ctx_cap;
+    int n_mtiles;  // ceil(G*L / 128) query tiles per (b, kv head)
+    int chunk;     // KV tiles per split
+    int nblk;      // ceil(L / 128) tiles of block keys
+    float scale_log2;
+    const int32_t* ctx_len;
+    __nv_bfloat16* out;
+    float* ws_o;   // split partials [splits][B][Hkv][n_mtiles*128][D] (nullptr: one split)
+    float* ws_ml;  // [splits][B][Hkv][n_mtiles*128][2] = (running max, running sum)
+    unsigned* status;
+    unsigned long long timeout_ns;
+};
+
+struct AttnMaps {
+    CUtensorMap q, k_ctx, v_ctx, k_blk, v_blk;
+};
+
+// Bytes of dynamic shared memory the attention kernel needs for head dim D.
+int attn_smem_bytes(int D);
+
+cudaError_t launch_block_attn(const AttnMaps& maps, const AttnParams& p, int D, int splits,
+                              cudaStream_t s);
+cudaError_t launch_attn_merge(const AttnParams& p, int D, cudaStream_t s);
+
+struct CommitParams {
+    const float* logits;
+    int B, L, V, k;
+    int slice;  // logits per CTA of a row's cluster (multiple of 4)
+    const uint8_t* masked;
+    int32_t* tok;
+    uint8_t* masked_out;
+    unsigned long long* key;  // [B*L]
+    int32_t* arg;             // [B*L]
+    unsigned* status;
+    unsigned long long timeout_ns;
+};
+
+constexpr int kCommitCluster = 8;       // CTAs sharing one logit row
+constexpr int kCommitThreads = 256;
+constexpr int kCommitSliceMax = 16384;  // fp32 logits per CTA (64 KB of shared memory)
+
+cudaError_t launch_commit(const CommitParams& p, cudaStream_t s);
+cudaError_t configure_commit_kernels();
+cudaError_t configure_attn_kernels();
+
+}  // namespace tt

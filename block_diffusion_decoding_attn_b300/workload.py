@@ -215,3 +215,31 @@ def random_mask(w: Workload, frac: float, seed: int = 0) -> np.ndarray:
     """A mask with about `frac` of the positions still masked (ragged per block)."""
     g = _rng(seed, w.wid, 99, 0)
     return (g.random(w.rows) < frac).astype(np.uint8)
+
+
+def attn_tensors(inp: AttnInputs, device="cuda", pin: bool = False) -> dict:
+    """The attention inputs as torch tensors (bf16 views of the bit patterns)."""
+    import torch
+
+    def t(a, bf16=True):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        if bf16:
+            x = x.view(torch.bfloat16)
+        if pin:
+            x = x.pin_memory()
+        return x.to(device, non_blocking=pin) if device != "cpu" else x
+
+    return dict(q=t(inp.q), k_blk=t(inp.k_blk), v_blk=t(inp.v_blk), k_ctx=t(inp.k_ctx),
+                v_ctx=t(inp.v_ctx), ctx_len=t(inp.ctx_len, bf16=False))
+
+
+def commit_tensors(inp: CommitInputs, device="cuda", pin: bool = False) -> dict:
+    import torch
+
+    def t(a):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        if pin:
+            x = x.pin_memory()
+        return x.to(device, non_blocking=pin) if device != "cpu" else x
+
+    return dict(logits=t(inp.logits), masked=t(inp.masked), tok=t(inp.tok))

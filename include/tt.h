@@ -1,0 +1,153 @@
+/*
+ * tt.h -- C ABI of the TwoTower denoising-step hot path on NVIDIA B300
+ * (sm_103a): the denoiser's block attention and the unmask/commit step.
+ *
+ * Source of the method: "Nemotron-Labs-TwoTower: Diffusion Language Modeling
+ * with Pretrained Autoregressive Context" (arXiv 2606.26493), Section 2.1
+ * (two-tower architecture, "Bidirectional Attention", Eq. 1) and Section 2.2
+ * ("Sampling", Algorithm 2, confidence unmasking).
+ *
+ * Conventions (all entry points):
+ *   - Plain C types only. Tensor arguments are DEVICE pointers to contiguous
+ *     row-major arrays with the shapes given below; the caller owns every
+ *     buffer, including the workspace. The library never allocates on the call
+ *     path (only tt_create allocates: a 4-byte device status word).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Calls are asynchronous on it.
+ *   - Return value: TT_OK, or a negative tt_status for an error detected on
+ *     the host before anything is launched (nothing is written then). The
+ *     message of the last host error of the calling thread is available from
+ *     tt_last_error().
+ *   - Errors detected on the device (a ctx_len outside [0, ctx_cap], a
+ *     pipeline wait that timed out) set bits of the handle's status word; read
+ *     and clear it with tt_get_error. Kernels never trap.
+ *   - A handle may be used from one host thread at a time. Calls that share a
+ *     workspace must be ordered on the GPU (same stream, or events).
+ */
+#ifndef TT_H_
+#define TT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TT_OK = 0,
+    TT_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer       */
+    TT_ERR_UNSUPPORTED = -2, /* a shape outside the supported set (see below)    */
+    TT_ERR_CUDA = -3,        /* a CUDA runtime or driver call failed             */
+    TT_ERR_DEVICE = -4,      /* tt_get_error: the device status word is non-zero */
+    TT_ERR_WORKSPACE = -5    /* workspace pointer missing or too small           */
+} tt_status;
+
+/* Bits of the device status word (tt_get_error). */
+#define TT_DEV_CTX_LEN_RANGE 1u /* a ctx_len[b] outside [0, ctx_cap] (it was clamped) */
+#define TT_DEV_WAIT_TIMEOUT 2u  /* a bounded pipeline wait gave up; outputs invalid    */
+
+typedef struct tt_context* tt_handle;
+
+/* Creates a handle bound to CUDA device `device` (made current while the
+ * library works on it). Allocates the device status word and sets kernel
+ * attributes. Returns TT_OK, TT_ERR_INVALID_ARG (handle NULL) or TT_ERR_CUDA
+ * (no such device, or it is not a compute capability 10.3 part). */
+int tt_create(tt_handle* handle, int device);
+
+/* Frees the handle. Synchronizes nothing: the caller makes sure no launch on
+ * the handle is still running. NULL is a no-op. */
+int tt_destroy(tt_handle handle);
+
+/* Reads and clears the device status word. Synchronizes the handle's device
+ * (cudaDeviceSynchronize). *device_status receives the TT_DEV_* bits (may be
+ * NULL). Returns TT_OK if no bit was set, TT_ERR_DEVICE if one was, TT_ERR_CUDA
+ * if the synchronization reported a CUDA error. */
+int tt_get_error(tt_handle handle, unsigned* device_status);
+
+/* Sets how long a pipeline wait inside a kernel may last before it gives up,
+ * sets TT_DEV_WAIT_TIMEOUT and lets the kernel wind down (default 1 s). */
+int tt_set_wait_timeout(tt_handle handle, unsigned long long nanoseconds);
+
+/* Human-readable name of a tt_status value. */
+const char* tt_status_string(int status);
+
+/* Message of the last host-side error raised on the calling thread ("" if none). */
+const char* tt_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Block attention -- Section 2.1, "Bidirectional Attention", Eq. (1):
+ *   Attn(Q_b^(i), [K_<b^ctx,(i); K_b^den,(i)], [V_<b^ctx,(i); V_b^den,(i)])
+ * Every query of the L-token noisy block takes ONE softmax over the
+ * concatenation of the context tower's layer-i keys for the ctx_len[b] clean
+ * positions before the block and the denoiser's own layer-i keys for the block,
+ * with no mask inside the block. Layer alignment (denoiser layer i reads
+ * context layer i) is the caller's choice of k_ctx / v_ctx: one call per layer.
+ * GQA: query head h uses KV head h / (Hq / Hkv).
+ *
+ * Layouts (bf16, row-major, contiguous, 16-byte aligned):
+ *   q      [B][L][Hq][D]        queries of the noisy block
+ *   k_blk  [B][L][Hkv][D]       the block's own keys      (denoiser tower)
+ *   v_blk  [B][L][Hkv][D]       the block's own values
+ *   k_ctx  [B][Hkv][ctx_cap][D] layer-i KV cache           (context tower)
+ *   v_ctx  [B][Hkv][ctx_cap][D]   positions >= ctx_len[b] are never used and
+ *                                 may hold anything, NaN included
+ *   ctx_len [B] int32, device    0 <= ctx_len[b] <= ctx_cap
+ *   out    [B][L][Hq][D]        bf16, written in full
+ * Arithmetic: bf16 products with fp32 accumulation (tcgen05), fp32 online
+ * softmax, probabilities rounded to bf16 for the P*V product, output rounded
+ * to bf16 (nearest even).
+ * Supported: D in {64, 128}; Hq % Hkv == 0 with Hq/Hkv a power of two <= 128;
+ * 1 <= L <= 65536; B >= 0 (B == 0 is a no-op); scale > 0 or 0 for 1/sqrt(D).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int B, L, Hq, Hkv, D, ctx_cap;
+    float scale;    /* softmax scale; 0 selects 1/sqrt(D) */
+    int num_splits; /* KV splits per (b, kv head, query tile); 0 = automatic */
+} tt_attn_desc;
+
+/* Workspace bytes tt_block_attn needs for `desc` on this handle's device
+ * (0 when no KV split is used). Returns 0 for an invalid desc as well. */
+size_t tt_block_attn_workspace_bytes(tt_handle handle, const tt_attn_desc* desc);
+
+int tt_block_attn(tt_handle handle, const tt_attn_desc* desc, const void* q, const void* k_blk,
+                  const void* v_blk, const void* k_ctx, const void* v_ctx,
+                  const int32_t* ctx_len, void* out, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
+/* ------------------------------------------------------------------------
+ * Unmask / commit -- Section 2.2, "Sampling", Algorithm 2 (ConfidenceSample),
+ * read as a fixed budget of k commits per block per step (the threshold rule
+ * with gamma > 1 and T = L/k steps).
+ * For every row r of block b with masked[r] == 1:
+ *   prediction a_r = lowest v with logits[r][v] == max_v logits[r][v]
+ *   key_r = sum_v rint(2^40 * e(RN32(logits[r][v] - max))), an integer;
+ *     e is an fp32 exponential fixed by this library (Cody-Waite reduction,
+ *     degree-7 Taylor polynomial, fused multiply-adds; within 1 ulp of exp
+ *     on [-30, 0], 0 below -30), so the key is bit-reproducible;
+ *     2^40 / key_r is the maximum softmax probability (the confidence) up to
+ *     a relative error below V * 2^-40 + 2^-22.
+ * Then per block the min(k, #masked) rows with the smallest (key, row) are
+ * committed: tok[r] = a_r, masked_out[r] = 0. Every other entry of tok is left
+ * untouched; masked_out[r] = masked[r] elsewhere.
+ *
+ *   logits     [B*L][V] fp32, device, 16-byte aligned, finite values
+ *   masked     [B*L] uint8 (0/1), device
+ *   tok        [B*L] int32, device, updated in place at committed rows
+ *   masked_out [B*L] uint8, device; may be the same buffer as masked
+ * Rows with masked[r] == 0 are not read. Supported: V % 4 == 0,
+ * 4 <= V <= 131072, 1 <= L <= 65536, k >= 1 (k >= #masked commits all).
+ * Workspace layout (after the call): uint64 key[B*L], then int32 arg[B*L],
+ * valid at rows that were masked on entry.
+ * ------------------------------------------------------------------------ */
+size_t tt_commit_workspace_bytes(int B, int L);
+
+int tt_commit(tt_handle handle, const float* logits, int B, int L, int V, const uint8_t* masked,
+              int k, int32_t* tok, uint8_t* masked_out, void* workspace, size_t workspace_bytes,
+              void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TT_H_ */

@@ -1,0 +1,115 @@
+"""GPU parity of tt_commit against the scalar CPU oracle, bit for bit.
+
+Unmask/commit, "Nemotron-Labs-TwoTower" Section 2.2, Algorithm 2, with a fixed
+budget of k commits per block per step. On identical fp32 logits the GPU and
+the oracle must agree exactly on the canonical confidence keys, the greedy
+predictions, the committed set (ascending-row tie-break) and the updated ids
+and mask.
+"""
+import numpy as np
+import pytest
+
+from block_diffusion_decoding_attn_b300 import workload as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tt():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_diffusion_decoding_attn_b300 as tt
+    from block_diffusion_decoding_attn_b300 import build
+    build.build()
+    return tt
+
+
+def _gpu_step(tt, logits, B, L, masked, k, tok, alias=False):
+    import torch
+    lg = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
+    m = torch.from_numpy(masked.copy()).cuda()
+    t = torch.from_numpy(tok.copy()).cuda()
+    mo = m if alias else None
+    t, mo, ws = tt.commit(lg, B, L, m, k, t, masked_out=mo)
+    torch.cuda.synchronize()
+    assert tt.handle().get_error() == 0
+    keys, args = tt.commit_keys(ws, B, L)
+    return (t.cpu().numpy(), mo.cpu().numpy(), keys.cpu().numpy().view(np.uint64),
+            args.cpu().numpy())
+
+
+def _check_step(tt, oracle_lib, logits, B, L, masked, k, tok, alias=False):
+    gt, gm, gk, ga = _gpu_step(tt, logits, B, L, masked, k, tok, alias)
+    ot, om, ok, oa = oracle_lib.commit(logits, B, L, masked, k, tok)
+    sel = masked == 1
+    np.testing.assert_array_equal(gk[sel], ok[sel])
+    np.testing.assert_array_equal(ga[sel], oa[sel])
+    np.testing.assert_array_equal(gt, ot)
+    np.testing.assert_array_equal(gm, om)
+    return ot, om
+
+
+def test_tiny_full_denoise_loop(tt, oracle_lib):
+    w = wl.WORKLOADS["tiny_c256_l32"]
+    tok = np.full(w.rows, -1, np.int32)
+    masked = np.ones(w.rows, np.uint8)
+    steps = 0
+    while masked.any():
+        lg = wl.logits(w, seed=0, step=steps)
+        tok, masked = _check_step(tt, oracle_lib, lg, w.B, w.L, masked, w.k, tok)
+        steps += 1
+    assert steps == 8
+
+
+@pytest.mark.parametrize("case", [
+    # B, L, V, k, mask fraction
+    (4, 32, 1024, 4, 1.0),
+    (3, 50, 1000, 7, 0.6),      # V not a multiple of the cluster slice
+    (2, 300, 4096, 64, 0.9),    # L above one warp per row group
+    (5, 16, 2048, 1, 0.7),      # mock autoregressive mode: k = 1
+    (2, 24, 512, 100, 0.5),     # k above #masked: commit all
+    (1, 1, 4, 1, 1.0),          # smallest shape
+    (2, 1030, 256, 9, 0.8),     # L above the select kernel's 1024 threads
+])
+def test_shapes_and_masks(tt, oracle_lib, case):
+    B, L, V, k, frac = case
+    w = wl.custom("c", B, L, 1, 1, 8, 8, (0,) * B, V=V, k=k)
+    lg = wl.logits(w, seed=11)
+    masked = wl.random_mask(w, frac, seed=5) if frac < 1 else np.ones(w.rows, np.uint8)
+    tok = np.arange(w.rows, dtype=np.int32) + 7
+    _check_step(tt, oracle_lib, lg, B, L, masked, k, tok)
+
+
+def test_ties_and_alias(tt, oracle_lib):
+    w = wl.custom("ties", 2, 40, 1, 1, 8, 8, (0, 0), V=2048, k=6)
+    lg = wl.logits(w, seed=12)
+    lg[3] = lg[10]                   # identical rows -> identical keys; row 3 first
+    lg[50] = lg[41]
+    lg[7, [100, 900]] = 40.0         # argmax tie -> lower vocab id
+    lg[8] = 0.0                      # flat row
+    lg[9, :] = -1e30
+    lg[9, 5] = 3.0                   # confidence 1 (other terms underflow to 0)
+    masked = np.ones(w.rows, np.uint8)
+    masked[[0, 44]] = 0
+    lg[0] = np.nan                   # unmasked rows are never read
+    tok = np.full(w.rows, -1, np.int32)
+    _check_step(tt, oracle_lib, lg, 2, 40, masked, 6, tok, alias=True)
+
+
+@pytest.mark.parametrize("name", ["b8_c4096_l32", "b16_c1024_l256", "b4_gen8k_32x256",
+                                  "b64_ragged8k32k_l64"])
+def test_full_workloads_first_step(tt, oracle_lib, name):
+    w = wl.WORKLOADS[name]
+    inp = wl.commit_inputs(w, seed=0)
+    _check_step(tt, oracle_lib, inp.logits, w.B, w.L, inp.masked, w.k, inp.tok)
+
+
+def test_b8_full_loop(tt, oracle_lib):
+    w = wl.WORKLOADS["b8_c4096_l32"]
+    tok = np.full(w.rows, -1, np.int32)
+    masked = np.ones(w.rows, np.uint8)
+    for step in range(w.steps_to_unmask):
+        lg = wl.logits(w, seed=0, step=step)
+        tok, masked = _check_step(tt, oracle_lib, lg, w.B, w.L, masked, w.k, tok)
+    assert not masked.any()
