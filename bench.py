@@ -85,49 +85,80 @@ def profiled_traffic(kernel, workload):
     return e["dram_bytes_per_launch"]
 
 
+class _Nvml:
+    """Minimal ctypes binding of NVML (libnvidia-ml ships with the driver)."""
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+
+    def handle(self, uuid, index):
+        ct = self.ct
+        h = ct.c_void_p()
+        if uuid and self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ct.byref(h)) == 0:
+            return h
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(index, ct.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return h
+
+    def sm_clock(self, h, max_clock=False):
+        v = self.ct.c_uint()
+        f = self.lib.nvmlDeviceGetMaxClockInfo if max_clock else self.lib.nvmlDeviceGetClockInfo
+        return v.value if f(h, 1, self.ct.byref(v)) == 0 else None  # 1 = NVML_CLOCK_SM
+
+    def reasons(self, h):
+        v = self.ct.c_ulonglong()
+        return v.value if self.lib.nvmlDeviceGetCurrentClocksEventReasons(h, self.ct.byref(v)) == 0 else 0
+
+
 class ClockSampler:
-    """Polls SM clock and throttle reasons through NVML while the timed region runs."""
+    """Polls SM clock and clock-event reasons through NVML while the timed region runs."""
 
     REASONS = {
-        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
-        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
-        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+        "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
+        "sync_boost": 0x10, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+        "hw_power_brake_slowdown": 0x80,
     }
 
-    def __init__(self, index, period=0.005):
+    def __init__(self, index, period=0.002):
         self.index, self.period = index, period
         self.samples, self.reasons = [], set()
         self._stop = threading.Event()
         self._t = None
         self.max_mhz = None
         self.ok = False
+        self.error = None
 
     def __enter__(self):
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            import torch
+            self._nv = _Nvml()
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.index).uuid)
+            self._h = self._nv.handle(uuid, self.index)
+            self.max_mhz = self._nv.sm_clock(self._h, max_clock=True)
             self.ok = True
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
-        except Exception:
+        except Exception as e:  # clocks are then reported as unknown
             self.ok = False
+            self.error = f"{type(e).__name__}: {e}"
         return self
 
     def _run(self):
-        nv = self._nv
-        while not self._stop.is_set():
-            try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                for name, bit in self.REASONS.items():
-                    if r & bit and name != "gpu_idle":
-                        self.reasons.add(name)
-            except Exception:
-                pass
-            time.sleep(self.period)
+        nv, h = self._nv, self._h
+        while True:
+            c = nv.sm_clock(h)
+            if c is not None:
+                self.samples.append(c)
+            r = nv.reasons(h)
+            for name, bit in self.REASONS.items():
+                if r & bit:
+                    self.reasons.add(name)
+            if self._stop.wait(self.period):
+                break
 
     def __exit__(self, *a):
         self._stop.set()
@@ -137,7 +168,7 @@ class ClockSampler:
     def summary(self):
         if not self.ok or not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                    "samples": len(self.samples)}
+                    "samples": len(self.samples), "error": self.error}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(self.reasons), "samples": len(self.samples)}
 
@@ -167,19 +198,20 @@ def cpu_oracle_step(w, inp, cinp, seqs, threads=0):
 
 
 def cpu_baseline(w, inp, cinp, budget_s=12.0):
+    """The oracle as it stands, on all host cores, for about `budget_s` seconds:
+    whole sequences of the same workload (all heads, the block's commit)."""
     cores = os.cpu_count() or 1
     t0 = time.perf_counter()
-    done = cpu_oracle_step(w, inp, cinp, [0])
+    cpu_oracle_step(w, inp, cinp, [0])  # calibration (also warms the caches)
+    per_seq = time.perf_counter() - t0
+    n = max(1, int(budget_s / max(per_seq, 1e-6)))
+    seqs = [i % w.B for i in range(n)]
     t1 = time.perf_counter()
-    per_seq = t1 - t0
-    n = max(1, min(w.B - 1, int(budget_s / max(per_seq, 1e-6)) - 1))
-    seqs = list(range(1, 1 + n))
-    t2 = time.perf_counter()
     done = cpu_oracle_step(w, inp, cinp, seqs)
-    dt = time.perf_counter() - t2
+    dt = time.perf_counter() - t1
     return {"value": done / dt, "unit": "block-tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {w.B} sequences ({done} block tokens, all {w.Hq} heads, "
-                      f"attention fp64 loops + scalar commit), {dt:.2f} s"}
+            "sample": f"{n} sequences of {w.L} block tokens (cycling over the batch of {w.B}; "
+                      f"all {w.Hq} heads, fp64 attention loops + scalar commit), {dt:.2f} s"}
 
 
 def run_reference(args, w):
@@ -243,7 +275,7 @@ def run_gpu(args, w):
     desc = tt.attn_desc(A["q"], A["k_ctx"])
     ws_a_n = tt.block_attn_workspace_bytes(desc, h)
     ws_a = torch.empty(max(ws_a_n, 256), dtype=torch.uint8, device=dev)
-    ws_c = torch.empty(max(tt.commit_workspace_bytes(w.B, w.L), 256), dtype=torch.uint8,
+    ws_c = torch.zeros(max(tt.commit_workspace_bytes(w.B, w.L), 256), dtype=torch.uint8,
                        device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)

@@ -197,7 +197,8 @@ def commit(logits, B: int, L: int, masked, k: int, tok, masked_out=None, workspa
 
     logits [B*L][V] float32, masked [B*L] uint8, tok [B*L] int32 (updated in
     place at committed rows). Returns (tok, masked_out, workspace); the
-    workspace holds key[B*L] (uint64) then arg[B*L] (int32).
+    workspace holds key[B*L] (uint64), arg[B*L] (int32) and the block tickets.
+    A caller-provided workspace must have been zero-filled before its first use.
     """
     import torch
     if logits.dtype != torch.float32 or not logits.is_cuda or not logits.is_contiguous():
@@ -209,7 +210,8 @@ def commit(logits, B: int, L: int, masked, k: int, tok, masked_out=None, workspa
         masked_out = torch.empty_like(masked)
     need = commit_workspace_bytes(B, L)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=logits.device)
+        # zero-filled: the per-block tickets must start at zero (calls keep them so)
+        workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=logits.device)
     _check(lib().tt_commit(h.ptr, _dev_ptr(logits), int(B), int(L), int(logits.shape[1]),
                            _dev_ptr(masked), int(k), _dev_ptr(tok), _dev_ptr(masked_out),
                            _dev_ptr(workspace), workspace.numel() * workspace.element_size(),

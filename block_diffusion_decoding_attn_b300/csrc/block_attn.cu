@@ -3,19 +3,25 @@
 // softmax over [context-tower keys 0..ctx_len-1 of this layer; the block's own
 // L keys], with no mask inside the block and GQA head sharing.
 //
-// One CTA owns one work unit (sequence b, KV head, 128-row query tile, KV
-// split). The G = Hq/Hkv query heads of a KV head are packed with the block
-// positions into the M dimension (row = l*G + g), so a K/V tile staged once in
-// shared memory feeds all of them.
+// One CTA owns one work unit: (sequence b, KV head, pair of 128-row query
+// tiles, KV split). The G = Hq/Hkv query heads of a KV head are packed with the
+// block positions into the M dimension (row = l*G + g), so each K/V tile staged
+// once in shared memory feeds 256 query rows.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: one query row per thread, reads S from TMEM, online
-//              softmax in fp32 (log2 domain), writes P (bf16) to shared memory,
-//              rescales O in TMEM when the running max grows by > 2^8
-//   warp 4     TMA producer: Q tile once, then K/V tiles into a 2-stage ring
-//   warp 5     MMA issuer: S = Q K^T and O += P V on tcgen05 (fp32 in TMEM);
-//              owns the TMEM allocation
-// TMEM columns: S double buffer at 0 and 128, O at 256 (D columns).
+// Warp roles (320 threads):
+//   warps 0-3  softmax of query tile A, warps 4-7 of tile B: one query row per
+//              thread; S from TMEM, online softmax in fp32 (log2 domain), P as
+//              bf16 back into TMEM over the first half of S; rescales O in TMEM
+//              when the running max grows by more than 2^8
+//   warp 8     TMA producer: Q tiles once, then K_j, V_j into a 5-slot ring
+//   warp 9     MMA issuer (tcgen05, fp32 accumulators in TMEM) and TMEM owner
+// TMEM columns: S_A 0-127, O_A 128-255, S_B 256-383, O_B 384-511. P_X lives in
+// columns 0-63 of S_X (two bf16 per column) and is the A operand of O_X += P V.
+// The tensor core runs the two tiles in ping-pong: while tile A's softmax runs
+// it computes tile B's P V and next S, and the other way round. tcgen05.mma
+// operations complete in issue order, so "S_X(j) complete" also means
+// "P V of tile X for KV tile j-1 complete": the softmax may then overwrite S_X
+// with P and rescale O_X without another wait.
 #include "ptx.cuh"
 #include "tt_internal.h"
 
@@ -23,21 +29,18 @@ namespace tt {
 
 namespace {
 
-constexpr int kStages = 2;
-constexpr float kRescaleThresh = 8.0f;  // log2 units
+constexpr int kRing = 5;               // K/V tile slots (K_j and V_j alternate)
+constexpr float kRescaleThresh = 8.0f; // log2 units
 
 template <int D>
 struct AttnLayout {
-    static constexpr int kTileBytes = kTile * D * 2;     // a Q, K or V tile (bf16)
-    static constexpr int kAtomBytes = kTile * 128;       // one 64-column swizzle atom column
-    static constexpr int kPBytes = kTile * kTile * 2;    // a P tile (bf16)
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTileBytes;
-    static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kP = kV + kStages * kTileBytes;
-    static constexpr int kBar = kP + 2 * kPBytes;
-    // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done[2], drain
-    static constexpr int kNumBars = 1 + 4 * kStages + 7;
+    static constexpr int kTileBytes = kTile * D * 2;  // a Q, K or V tile (bf16)
+    static constexpr int kAtomBytes = kTile * 128;    // one 64-column swizzle atom column
+    static constexpr int kQ = 0;                      // Q_A, then Q_B
+    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kBar = kRingOff + kRing * kTileBytes;
+    // q_full, full[kRing], empty[kRing], s_full[2], p_full[2], o_final[2], drain
+    static constexpr int kNumBars = 1 + 2 * kRing + 7;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for the 1024-byte alignment
@@ -56,7 +59,7 @@ __device__ __forceinline__ KvTile kv_tile(int j, int nc, int C, int L) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_kc,
                       const __grid_constant__ CUtensorMap tm_vc,
@@ -68,8 +71,8 @@ __global__ void __launch_bounds__(192, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mtile = blockIdx.x % p.n_mtiles;
-    const int split = blockIdx.x / p.n_mtiles;
+    const int pair = blockIdx.x % p.n_pairs;
+    const int split = blockIdx.x / p.n_pairs;
     const int kvh = blockIdx.y, b = blockIdx.z;
 
     int C = p.ctx_len[b];
@@ -86,33 +89,29 @@ __global__ void __launch_bounds__(192, 1)
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::kBar);
     uint64_t* q_full = bars;
-    uint64_t* k_full = bars + 1;
-    uint64_t* k_empty = k_full + kStages;
-    uint64_t* v_full = k_empty + kStages;
-    uint64_t* v_empty = v_full + kStages;
-    uint64_t* s_full = v_empty + kStages;
+    uint64_t* full = bars + 1;
+    uint64_t* empty = full + kRing;
+    uint64_t* s_full = empty + kRing;
     uint64_t* p_full = s_full + 2;
-    uint64_t* pv_done = p_full + 2;
-    uint64_t* drain = pv_done + 2;
+    uint64_t* o_final = p_full + 2;
+    uint64_t* drain = o_final + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::kTmemSlot);
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], 128);
-            mbar_init(&pv_done[s], 1);
+            mbar_init(&o_final[s], 1);
         }
         mbar_init(drain, 1);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -122,7 +121,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t limit = p.timeout_ns;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -130,122 +129,145 @@ __global__ void __launch_bounds__(192, 1)
             tma_prefetch_desc(&tm_vc);
             tma_prefetch_desc(&tm_kb);
             tma_prefetch_desc(&tm_vb);
+            mbar_arrive_expect_tx(q_full, 2 * Lay::kTileBytes);
+            const int rows_l = kTile / p.G;  // block positions per query tile
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_5d(sm + Lay::kQ + t * Lay::kTileBytes + c * Lay::kAtomBytes, &tm_q,
+                                q_full, c * 64, 0, kvh, (2 * pair + t) * rows_l, b);
             bool ok = true;
-            uint8_t* sq = sm + Lay::kQ;
-            mbar_arrive_expect_tx(q_full, Lay::kTileBytes);
-            const int l0 = mtile * (kTile / p.G);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_5d(sq + c * Lay::kAtomBytes, &tm_q, q_full, c * 64, 0, kvh, l0, b);
-            int k_issued = 0, v_issued = 0;
-            for (int i = 0; i < n; ++i) {
-                const int st = i % kStages;
-                const uint32_t ph = (i / kStages) & 1;
-                const KvTile t = kv_tile(t0 + i, nc, C, p.L);
-                if (i >= kStages && !mbar_wait(&k_empty[st], ph ^ 1, limit)) { ok = false; break; }
-                uint8_t* sk = sm + Lay::kK + st * Lay::kTileBytes;
-                mbar_arrive_expect_tx(&k_full[st], Lay::kTileBytes);
+            int issued = 0;  // ring loads issued: K_j is load 2j, V_j is load 2j+1
+            for (int li = 0; li < 2 * n; ++li) {
+                const int slot = li % kRing;
+                if (li >= kRing && !mbar_wait(&empty[slot], ((li / kRing) & 1) ^ 1, limit)) {
+                    ok = false;
+                    break;
+                }
+                const KvTile t = kv_tile(t0 + (li >> 1), nc, C, p.L);
+                const bool is_v = li & 1;
+                uint8_t* dst = sm + Lay::kRingOff + slot * Lay::kTileBytes;
+                mbar_arrive_expect_tx(&full[slot], Lay::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                     if (t.is_ctx)
-                        tma_load_3d(sk + c * Lay::kAtomBytes, &tm_kc, &k_full[st], c * 64, t.base,
-                                    b * p.Hkv + kvh);
+                        tma_load_3d(dst + c * Lay::kAtomBytes, is_v ? &tm_vc : &tm_kc, &full[slot],
+                                    c * 64, t.base, b * p.Hkv + kvh);
                     else
-                        tma_load_4d(sk + c * Lay::kAtomBytes, &tm_kb, &k_full[st], c * 64, kvh,
-                                    t.base, b);
+                        tma_load_4d(dst + c * Lay::kAtomBytes, is_v ? &tm_vb : &tm_kb, &full[slot],
+                                    c * 64, kvh, t.base, b);
                 }
-                k_issued = i + 1;
-                if (i >= kStages && !mbar_wait(&v_empty[st], ph ^ 1, limit)) { ok = false; break; }
-                uint8_t* sv = sm + Lay::kV + st * Lay::kTileBytes;
-                mbar_arrive_expect_tx(&v_full[st], Lay::kTileBytes);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    if (t.is_ctx)
-                        tma_load_3d(sv + c * Lay::kAtomBytes, &tm_vc, &v_full[st], c * 64, t.base,
-                                    b * p.Hkv + kvh);
-                    else
-                        tma_load_4d(sv + c * Lay::kAtomBytes, &tm_vb, &v_full[st], c * 64, kvh,
-                                    t.base, b);
-                }
-                v_issued = i + 1;
+                issued = li + 1;
             }
             if (!ok) {
                 atomicOr(p.status, kDevWaitTimeout);
                 // Let the copies already issued land before the CTA can exit.
                 mbar_wait(q_full, 0, limit);
-                for (int i = k_issued - kStages < 0 ? 0 : k_issued - kStages; i < k_issued; ++i)
-                    mbar_wait(&k_full[i % kStages], (i / kStages) & 1, limit);
-                for (int i = v_issued - kStages < 0 ? 0 : v_issued - kStages; i < v_issued; ++i)
-                    mbar_wait(&v_full[i % kStages], (i / kStages) & 1, limit);
+                for (int li = issued - kRing < 0 ? 0 : issued - kRing; li < issued; ++li)
+                    mbar_wait(&full[li % kRing], (li / kRing) & 1, limit);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t idesc_qk = idesc_bf16(kTile, kTile, 0, 0);
         constexpr uint32_t idesc_pv = idesc_bf16(kTile, D, 0, 1);
-        bool ok = mbar_wait(q_full, 0, limit);
         const uint32_t sq = smem_u32(sm + Lay::kQ);
-        for (int i = 0; i <= n && ok; ++i) {
-            if (i < n) {
-                const int st = i % kStages;
-                if (!mbar_wait(&k_full[st], (i / kStages) & 1, limit)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t sk = smem_u32(sm + Lay::kK + st * Lay::kTileBytes);
-                    const uint32_t d_s = tmem + (i & 1) * kTile;
+        const uint32_t ring = smem_u32(sm + Lay::kRingOff);
+        const uint32_t col_s[2] = {0u, 2u * kTile};
+        const uint32_t col_o[2] = {static_cast<uint32_t>(kTile), 3u * kTile};
+        auto wait_slot = [&](int li) {
+            return mbar_wait(&full[li % kRing], (li / kRing) & 1, limit);
+        };
+        // S_X = Q_X K^T for the K tile in ring load li
+        auto issue_s = [&](int x, int li) {
+            const uint32_t sk = ring + (li % kRing) * Lay::kTileBytes;
+            const uint32_t sqx = sq + x * Lay::kTileBytes;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * Lay::kAtomBytes + (kk & 3) * 32;
-                        tc_mma_ss(d_s, sdesc_sw128(sq + off, 16, 1024),
-                                  sdesc_sw128(sk + off, 16, 1024), idesc_qk, kk > 0);
-                    }
-                    tc_commit(&s_full[i & 1]);
-                    tc_commit(&k_empty[st]);
-                }
-                __syncwarp();
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * Lay::kAtomBytes + (kk & 3) * 32;
+                tc_mma_ss(tmem + col_s[x], sdesc_sw128(sqx + off, 16, 1024),
+                          sdesc_sw128(sk + off, 16, 1024), idesc_qk, kk > 0);
             }
-            if (i >= 1) {
-                const int t = i - 1;
-                const int pb = t & 1, vs = t % kStages;
-                if (!mbar_wait(&p_full[pb], (t >> 1) & 1, limit) ||
-                    !mbar_wait(&v_full[vs], (t / kStages) & 1, limit)) {
-                    ok = false;
-                    break;
-                }
-                const KvTile kt = kv_tile(t0 + t, nc, C, p.L);
-                if (kt.is_ctx && kt.valid < kTile) {
-                    // Cache rows past ctx_len may hold anything (even NaN);
-                    // P is 0 there, but 0 * NaN is not, so zero those V rows.
-                    uint8_t* sv = sm + Lay::kV + vs * Lay::kTileBytes;
-                    const int rows = kTile - kt.valid;
-                    for (int u = lane; u < rows * 8 * (D / 64); u += 32) {
-                        const int c = u / (rows * 8);
-                        const int rem = u % (rows * 8);
-                        const int r = kt.valid + rem / 8;
-                        *reinterpret_cast<uint4*>(sv + c * Lay::kAtomBytes + r * 128 +
-                                                  (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t sp = smem_u32(sm + Lay::kP + pb * Lay::kPBytes);
-                    const uint32_t sv = smem_u32(sm + Lay::kV + vs * Lay::kTileBytes);
+        };
+        // O_X (+)= P_X V for the V tile in ring load li
+        auto issue_pv = [&](int x, int li, bool first) {
+            const uint32_t sv = ring + (li % kRing) * Lay::kTileBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        const uint64_t ad =
-                            sdesc_sw128(sp + (kk >> 2) * Lay::kAtomBytes + (kk & 3) * 32, 16, 1024);
-                        // V is MN-major (d contiguous): 16 keys = two 8-row atoms;
-                        // the next 64 columns of d sit one atom column further.
-                        const uint64_t bd = sdesc_sw128(sv + kk * 2048, Lay::kAtomBytes, 1024);
-                        tc_mma_ss(tmem + 2 * kTile, ad, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&pv_done[pb]);
-                    tc_commit(&v_empty[vs]);
-                }
-                __syncwarp();
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+                // V is MN-major (d contiguous): 16 keys = two 8-row atoms; the
+                // next 64 columns of d sit one atom column further.
+                const uint64_t bd = sdesc_sw128(sv + kk * 2048, Lay::kAtomBytes, 1024);
+                tc_mma_ts(tmem + col_o[x], tmem + col_s[x] + kk * 8, bd, idesc_pv,
+                          (!first || kk > 0) ? 1u : 0u);
             }
+        };
+        auto zero_tail = [&](int j, int li) {
+            // Cache rows past ctx_len may hold anything (even NaN); P is 0
+            // there, but 0 * NaN is not, so zero those V rows.
+            const KvTile kt = kv_tile(t0 + j, nc, C, p.L);
+            if (kt.is_ctx && kt.valid < kTile) {
+                uint8_t* sv = sm + Lay::kRingOff + (li % kRing) * Lay::kTileBytes;
+                const int rows = kTile - kt.valid;
+                for (int u = lane; u < rows * 8 * (D / 64); u += 32) {
+                    const int c = u / (rows * 8);
+                    const int rem = u % (rows * 8);
+                    const int r = kt.valid + rem / 8;
+                    *reinterpret_cast<uint4*>(sv + c * Lay::kAtomBytes + r * 128 + (rem % 8) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+        };
+
+        bool ok = mbar_wait(q_full, 0, limit) && wait_slot(0);
+        if (ok) {
+            tc_fence_after();
+            if (lane == 0) {
+                issue_s(0, 0);
+                tc_commit(&s_full[0]);
+                issue_s(1, 0);
+                tc_commit(&s_full[1]);
+                tc_commit(&empty[0]);
+            }
+            __syncwarp();
+        }
+        for (int j = 0; j < n && ok; ++j) {
+            const int lv = 2 * j + 1, lk = 2 * j + 2;
+            // ---- tile A
+            if (!mbar_wait(&p_full[0], j & 1, limit) || !wait_slot(lv)) { ok = false; break; }
+            zero_tail(j, lv);
+            tc_fence_after();
+            if (lane == 0) issue_pv(0, lv, j == 0);
+            __syncwarp();
+            const bool more = j + 1 < n;
+            if (more && !wait_slot(lk)) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) {
+                if (more) {
+                    issue_s(0, lk);
+                    tc_commit(&s_full[0]);
+                } else {
+                    tc_commit(&o_final[0]);
+                }
+            }
+            __syncwarp();
+            // ---- tile B
+            if (!mbar_wait(&p_full[1], j & 1, limit)) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) {
+                issue_pv(1, lv, j == 0);
+                tc_commit(&empty[lv % kRing]);
+                if (more) {
+                    issue_s(1, lk);
+                    tc_commit(&s_full[1]);
+                    tc_commit(&empty[lk % kRing]);
+                } else {
+                    tc_commit(&o_final[1]);
+                }
+            }
+            __syncwarp();
         }
         if (!ok && lane == 0) atomicOr(p.status, kDevWaitTimeout);
         // No MMA may still be running when the TMEM is released.
@@ -254,133 +276,116 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait(drain, 0, limit);
     } else {
         // ------------------------------------------------------------ softmax
-        const int row = warp * 32 + lane;
-        const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const int x = warp >> 2;               // query tile
+        const int row = (warp & 3) * 32 + lane;  // TMEM lane = row of the tile
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t ts = tmem + lane_off + (x ? 2u * kTile : 0u);
+        const uint32_t to = tmem + lane_off + (x ? 3u * kTile : static_cast<uint32_t>(kTile));
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int i = 0; i < n; ++i) {
-            const int sb = i & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (i >> 1) & 1, limit));
+        for (int j = 0; j < n; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, limit));
             if (!ok) break;
             tc_fence_after();
             float s[kTile];
+            {
+                uint32_t r[kTile];
+                tmem_ld128(ts, r);
 #pragma unroll
-            for (int c4 = 0; c4 < kTile / 32; ++c4) {
-                uint32_t r[32];
-                tmem_ld32(tl + sb * kTile + c4 * 32, r);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) s[c4 * 32 + j] = __uint_as_float(r[j]);
+                for (int c = 0; c < kTile; ++c) s[c] = __uint_as_float(r[c]);
             }
-            const KvTile kt = kv_tile(t0 + i, nc, C, p.L);
-            float mx = -INFINITY;
+            const KvTile kt = kv_tile(t0 + j, nc, C, p.L);
+            if (kt.valid < kTile) {
 #pragma unroll
-            for (int c = 0; c < kTile; ++c) {
-                s[c] = (c < kt.valid) ? s[c] : -INFINITY;
-                mx = fmaxf(mx, s[c]);
+                for (int c = 0; c < kTile; ++c) s[c] = (c < kt.valid) ? s[c] : -INFINITY;
             }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c + 1 < kTile; c += 2) mx = max3f(mx, s[c], s[c + 1]);
+            mx = fmaxf(mx, s[kTile - 1]);
             const float m_tile = mx * sl2;
-            if (i == 0) {
+            if (j == 0) {
                 m_run = m_tile;
-            } else if (m_tile > m_run + kRescaleThresh) {
-                const float alpha = ex2_approx(m_run - m_tile);
-                m_run = m_tile;
+            } else if (__any_sync(0xffffffffu, m_tile > m_run + kRescaleThresh)) {
+                // Warp-uniform (the TMEM accesses are warp-collective): every
+                // lane moves to its new max; alpha is 1 where nothing changed.
+                // O_X is final for KV tile j-1 (S_X(j) completed after it).
+                const float m_new = fmaxf(m_run, m_tile);
+                const float alpha = ex2_approx(m_run - m_new);
+                m_run = m_new;
                 l_run *= alpha;
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, limit));
-                if (!ok) break;
-                tc_fence_after();
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
                     uint32_t r[32];
-                    tmem_ld32(tl + 2 * kTile + c4 * 32, r);
+                    tmem_ld32(to + c4 * 32, r);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-                    tmem_st32(tl + 2 * kTile + c4 * 32, r);
+                    for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+                    tmem_st32(to + c4 * 32, r);
                 }
             }
-            if (i >= 2) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[sb], ((i - 2) >> 1) & 1, limit));
-                if (!ok) break;
-            }
-            uint8_t* pbuf = sm + Lay::kP + sb * Lay::kPBytes + row * 128;
             const float neg_m = -m_run;
-            float lsum = 0.f;
+            float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int h = 0; h < 2; ++h) {  // P in two halves of 64 keys (32 columns each)
+                uint32_t pk[32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    float e[8];
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) {
-                        e[x] = ex2_approx(fmaf(s[c * 64 + u * 8 + x], sl2, neg_m));
-                        lsum += e[x];
-                    }
-                    const uint4 v = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                                               pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
-                    *reinterpret_cast<uint4*>(pbuf + c * Lay::kAtomBytes + ((u ^ (row & 7)) << 4)) = v;
+                for (int c = 0; c < 64; c += 2) {
+                    float a0, a1;
+                    fma2(a0, a1, s[h * 64 + c], s[h * 64 + c + 1], sl2, sl2, neg_m, neg_m);
+                    const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                    add2(sum0, sum1, sum0, sum1, e0, e1);
+                    pk[c >> 1] = pack_bf16x2(e0, e1);
                 }
+                tmem_st32(ts + h * 32, pk);  // P over the first 64 columns of S_X
             }
-            l_run += lsum;
-            fence_proxy_async_smem();
+            l_run += sum0 + sum1;
             tc_fence_before();
-            mbar_arrive(&p_full[sb]);
+            mbar_arrive(&p_full[x]);
         }
-        if (ok)
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, limit));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_final[x], 0, limit));
         if (!ok) {
             if (lane == 0) atomicOr(p.status, kDevWaitTimeout);
         } else {
             tc_fence_after();
-            const int m = mtile * kTile + row;
+            const int m = (2 * pair + x) * kTile + row;
             const int l = m / p.G, g = m % p.G;
             const bool live = l < p.L;
-            if (nsplit_b == 1) {
-                const float inv = 1.f / l_run;
-                __nv_bfloat16* dst =
-                    p.out + ((static_cast<size_t>(b) * p.L + l) * p.Hq + kvh * p.G + g) * D;
+            uint32_t r[kTile];
+            tmem_ld128(to, r);  // O (the first D columns)
+            if (live) {
+                if (nsplit_b == 1) {
+                    const float inv = 1.f / l_run;
+                    __nv_bfloat16* dst =
+                        p.out + ((static_cast<size_t>(b) * p.L + l) * p.Hq + kvh * p.G + g) * D;
 #pragma unroll
-                for (int c4 = 0; c4 < D / 32; ++c4) {
-                    uint32_t r[32];
-                    tmem_ld32(tl + 2 * kTile + c4 * 32, r);
-                    if (live) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            const uint4 v = make_uint4(
-                                pack_bf16x2(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv));
-                            *reinterpret_cast<uint4*>(dst + c4 * 32 + j) = v;
-                        }
+                    for (int c = 0; c < D; c += 8) {
+                        const uint4 v = make_uint4(
+                            pack_bf16x2(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(r[c + 2]) * inv, __uint_as_float(r[c + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(r[c + 4]) * inv, __uint_as_float(r[c + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(r[c + 6]) * inv, __uint_as_float(r[c + 7]) * inv));
+                        *reinterpret_cast<uint4*>(dst + c) = v;
                     }
-                }
-            } else {
-                const size_t prow =
-                    ((static_cast<size_t>(split) * p.B + b) * p.Hkv + kvh) *
-                        (static_cast<size_t>(p.n_mtiles) * kTile) + m;
-                float* dst = p.ws_o + prow * D;
+                } else {
+                    const size_t prow =
+                        ((static_cast<size_t>(split) * p.B + b) * p.Hkv + kvh) *
+                            (static_cast<size_t>(p.n_mtiles) * kTile) + m;
+                    float* dst = p.ws_o + prow * D;
 #pragma unroll
-                for (int c4 = 0; c4 < D / 32; ++c4) {
-                    uint32_t r[32];
-                    tmem_ld32(tl + 2 * kTile + c4 * 32, r);
-                    if (live) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(dst + c4 * 32 + j) =
-                                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                    }
+                    for (int c = 0; c < D; c += 4)
+                        *reinterpret_cast<float4*>(dst + c) =
+                            make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
+                                        __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+                    *reinterpret_cast<float2*>(p.ws_ml + prow * 2) = make_float2(m_run, l_run);
                 }
-                if (live) *reinterpret_cast<float2*>(p.ws_ml + prow * 2) = make_float2(m_run, l_run);
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -438,8 +443,8 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
 
 template <int D>
 cudaError_t launch_attn_impl(const AttnMaps& m, const AttnParams& p, int splits, cudaStream_t s) {
-    dim3 grid(p.n_mtiles * splits, p.Hkv, p.B);
-    block_attn_kernel<D><<<grid, 192, AttnLayout<D>::kAlloc, s>>>(m.q, m.k_ctx, m.v_ctx, m.k_blk,
+    dim3 grid(p.n_pairs * splits, p.Hkv, p.B);
+    block_attn_kernel<D><<<grid, 320, AttnLayout<D>::kAlloc, s>>>(m.q, m.k_ctx, m.v_ctx, m.k_blk,
                                                                   m.v_blk, p);
     return cudaGetLastError();
 }

@@ -1,29 +1,34 @@
 // Unmask/commit step of the TwoTower sampler ("Nemotron-Labs-TwoTower",
 // Section 2.2, Algorithm 2, confidence unmasking) with a fixed budget of k
-// commits per block per step.
+// commits per block per step. One launch:
 //
-// Kernel 1 (commit_rows_kernel), one 8-CTA cluster per still-masked row:
-//   each CTA bulk-copies its 1/8 slice of the fp32 logit row into shared
-//   memory (TMA, evict-first), finds max / first argmax, the cluster agrees
-//   on the row maximum m through distributed shared memory, then each CTA
-//   sums the canonical fixed-point terms q(l_v - m) of its slice from shared
-//   memory and CTA 0 adds the eight partial sums:
-//       key[r] = sum_v rint(2^40 * e(RN32(l_v - m))),  arg[r] = first argmax
-//   The sum is an integer, so the key does not depend on the reduction order
-//   and matches a scalar CPU loop bit for bit. key / 2^40 = 1 / (max softmax
-//   probability) up to the rounding of e; smaller key = more confident.
-// Kernel 2 (commit_select_kernel), one CTA per block: rank every masked row
-//   by (key, row) and commit the first min(k, #masked): tok[r] = arg[r],
-//   masked_out[r] = 0.
+// One 8-CTA cluster per row: each CTA bulk-copies its 1/8 slice of the fp32
+// logit row into shared memory (TMA, evict-first) and finds the slice's max
+// and first argmax; the cluster agrees on the row maximum m through
+// distributed shared memory; each CTA then sums the canonical fixed-point
+// terms q(l_v - m) of its slice from shared memory and CTA 0 adds the eight
+// partial sums:
+//     key[r] = sum_v rint(2^40 * e(RN32(l_v - m))),  arg[r] = first argmax
+// The sum is an integer, so the key does not depend on the reduction order and
+// matches a scalar CPU loop bit for bit. key / 2^40 = 1 / (max softmax
+// probability) up to the rounding of e; smaller key = more confident.
+// Every row's cluster then takes a ticket for its block; the cluster that
+// takes the last ticket ranks the block's masked rows by (key, row) and
+// commits the first min(k, #masked): tok[r] = arg[r], masked_out[r] = 0.
 //
 // e(x) is an fp32 exponential defined for this purpose (Cody and Waite range
 // reduction, then the degree-7 Taylor polynomial of exp, all with
 // round-to-nearest fused multiply-adds):
 //   x < -30 -> term 0
-//   t = RN(x * log2(e)), n = rint(t)
+//   n = nearest integer (ties to even) to the exact product x * log2(e)
 //   r = fma(-n, C1, x), r = fma(-n, C2, r)     C1 = RN32(ln 2), C2 = RN32(ln 2 - C1)
 //   p = c7; p = fma(p, r, c_j), j = 6..0       c_j = RN32(1 / j!)
 //   term = rint(p * 2^(n + 40))
+// The term is formed without any float-to-64-bit conversion (those run on the
+// FP64 pipe, which is narrow on this part): the polynomial carries the 2^40
+// factor in its coefficients (exact power-of-two scaling), 2^n is added to the
+// exponent field, and rint splits into a multiple of 2^20 plus a remainder,
+// both read out of the bits of exact fp32 sums.
 #include <cooperative_groups.h>
 
 #include "ptx.cuh"
@@ -35,35 +40,46 @@ namespace tt {
 
 namespace {
 
-// RN32(1/ln 2), RN32(ln 2), RN32(ln 2 - RN32(ln 2)), RN32(1/j!)
+// RN32(1/ln 2), RN32(ln 2), RN32(ln 2 - RN32(ln 2)); 2^40 * RN32(1/j!)
 constexpr float kLog2e = 0x1.715476p+0f;
 constexpr float kLn2Hi = 0x1.62e430p-1f;
 constexpr float kLn2Lo = -0x1.05c610p-29f;
-constexpr float kInvFact2 = 0x1.000000p-1f;
-constexpr float kInvFact3 = 0x1.555556p-3f;
-constexpr float kInvFact4 = 0x1.555556p-5f;
-constexpr float kInvFact5 = 0x1.111112p-7f;
-constexpr float kInvFact6 = 0x1.6c16c2p-10f;
-constexpr float kInvFact7 = 0x1.a01a02p-13f;
+constexpr float kC0 = 0x1.000000p+40f;
+constexpr float kC2 = 0x1.000000p+39f;
+constexpr float kC3 = 0x1.555556p+37f;
+constexpr float kC4 = 0x1.555556p+35f;
+constexpr float kC5 = 0x1.111112p+33f;
+constexpr float kC6 = 0x1.6c16c2p+30f;
+constexpr float kC7 = 0x1.a01a02p+27f;
+constexpr float kMagic23 = 0x1.8p+23f;  // fp32 sums in [2^23, 2^24) have ulp 1
+constexpr float kMagic43 = 0x1.8p+43f;  // ... in [2^43, 2^44) have ulp 2^20
+constexpr int kMagic23Bits = 0x4B400000;
+constexpr int kMagic43Bits = 0x55400000;
 
-// Fixed-point term rint(2^40 * e(x)) for x <= 0; explicit round-to-nearest
-// intrinsics so that no multiply-add is contracted differently.
-__device__ __forceinline__ unsigned long long fixed_term(float x) {
-    const float xc = fmaxf(x, -31.0f);
-    const float n = rintf(__fmul_rn(xc, kLog2e));
+// Adds rint(2^40 * e(x)) for x <= 0 to the pair (hi, lo): term = hi * 2^20 + lo.
+// Explicit round-to-nearest intrinsics, so nothing is contracted differently.
+__device__ __forceinline__ void add_fixed_term(float x, unsigned& hi, int& lo) {
+    const float xc = fmaxf(x, -31.0f);  // terms below -30 are 0 either way
+    const float nb = __fmaf_rn(xc, kLog2e, kMagic23);  // 1.5*2^23 + n
+    const float n = __fsub_rn(nb, kMagic23);
     float r = __fmaf_rn(-n, kLn2Hi, xc);
     r = __fmaf_rn(-n, kLn2Lo, r);
-    float p = kInvFact7;
-    p = __fmaf_rn(p, r, kInvFact6);
-    p = __fmaf_rn(p, r, kInvFact5);
-    p = __fmaf_rn(p, r, kInvFact4);
-    p = __fmaf_rn(p, r, kInvFact3);
-    p = __fmaf_rn(p, r, kInvFact2);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    const float scale = __int_as_float((static_cast<int>(n) + 40 + 127) << 23);  // 2^(n+40)
-    const unsigned long long q = __float2ull_rn(__fmul_rn(p, scale));
-    return x < -30.0f ? 0ull : q;
+    float p = kC7;
+    p = __fmaf_rn(p, r, kC6);
+    p = __fmaf_rn(p, r, kC5);
+    p = __fmaf_rn(p, r, kC4);
+    p = __fmaf_rn(p, r, kC3);
+    p = __fmaf_rn(p, r, kC2);
+    p = __fmaf_rn(p, r, kC0);
+    p = __fmaf_rn(p, r, kC0);  // 2^40 * p(r), in [2^39.5, 2^40.5]
+    // y = p * 2^n: add n to the exponent field; (bits(nb) << 23) == (n << 23) mod 2^32.
+    const float y = __int_as_float(__float_as_int(p) + (__float_as_int(nb) << 23));
+    const float a = __fadd_rn(y, kMagic43);  // 1.5*2^43 + 2^20 * round(y / 2^20)
+    const float yh = __fsub_rn(a, kMagic43);
+    const float rem = __fsub_rn(y, yh);       // exact, |rem| <= 2^19
+    const float b = __fadd_rn(rem, kMagic23);  // 1.5*2^23 + rint(rem)
+    hi += static_cast<unsigned>(__float_as_int(a) - kMagic43Bits);
+    lo += __float_as_int(b) - kMagic23Bits;
 }
 
 struct ArgMax {
@@ -78,127 +94,21 @@ __device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
 
 constexpr int kPieces = 4;  // bulk copies per slice, each with its own barrier
 
-__global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kCommitThreads)
-    commit_rows_kernel(const CommitParams p) {
-    extern __shared__ __align__(128) float slice[];
-    __shared__ __align__(8) uint64_t bars[kPieces];
-    __shared__ ArgMax red_am[kCommitThreads / 32];
-    __shared__ unsigned long long red_s[kCommitThreads / 32];
-    __shared__ ArgMax cta_am;               // this CTA's (max, argmax), read by the cluster
-    __shared__ unsigned long long cta_sum;  // this CTA's partial key, read by rank 0
-    __shared__ ArgMax row_am;
-
-    cg::cluster_group cluster = cg::this_cluster();
-    const int row = blockIdx.x / kCommitCluster;
-    const unsigned rank = cluster.block_rank();
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (!p.masked[row]) return;  // uniform over the cluster: all its CTAs read the same flag
-
-    const int v0 = static_cast<int>(rank) * p.slice;
-    const int cnt = max(0, min(p.slice, p.V - v0));  // multiple of 4
-    const float* src = p.logits + static_cast<size_t>(row) * p.V + v0;
-    const int per = (((cnt + kPieces - 1) / kPieces) + 3) & ~3;  // floats per piece
-
-    if (tid == 0) {
-        for (int i = 0; i < kPieces; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
-        const uint64_t pol = l2_policy_evict_first();
-        for (int i = 0; i < kPieces; ++i) {
-            const int lo = i * per, hi = min(cnt, lo + per);
-            if (hi > lo) {
-                mbar_arrive_expect_tx(&bars[i], (hi - lo) * 4);
-                bulk_load(slice + lo, src + lo, (hi - lo) * 4, &bars[i], pol);
-            }
-        }
-    }
-
-    // Pass 1: max and first argmax of the slice, piece by piece as it lands.
-    ArgMax am{-INFINITY, 0x7fffffff};
-    bool ok = true;
-    for (int i = 0; i < kPieces; ++i) {
-        const int lo = i * per, hi = min(cnt, lo + per);
-        if (hi <= lo) break;
-        if (!mbar_wait(&bars[i], 0, p.timeout_ns)) { ok = false; break; }
-        for (int e = lo + tid * 4; e < hi; e += kCommitThreads * 4) {
-            const float4 x = *reinterpret_cast<const float4*>(slice + e);
-            if (x.x > am.v) { am.v = x.x; am.i = v0 + e; }
-            if (x.y > am.v) { am.v = x.y; am.i = v0 + e + 1; }
-            if (x.z > am.v) { am.v = x.z; am.i = v0 + e + 2; }
-            if (x.w > am.v) { am.v = x.w; am.i = v0 + e + 3; }
-        }
-    }
-    if (!ok) {
-        if (tid == 0) atomicOr(p.status, kDevWaitTimeout);
-        // Let every copy already issued land before this CTA can exit.
-        for (int i = 0; i < kPieces; ++i)
-            if (min(cnt, i * per + per) > i * per) mbar_wait(&bars[i], 0, p.timeout_ns);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        ArgMax other{__shfl_xor_sync(0xffffffffu, am.v, o), __shfl_xor_sync(0xffffffffu, am.i, o)};
-        am = better(am, other);
-    }
-    if (lane == 0) red_am[warp] = am;
-    __syncthreads();
-    if (tid == 0) {
-        ArgMax a = red_am[0];
-        for (int w = 1; w < kCommitThreads / 32; ++w) a = better(a, red_am[w]);
-        cta_am = a;
-    }
-    cluster.sync();
-    if (tid == 0) {
-        ArgMax a{-INFINITY, 0x7fffffff};
-        for (int r = 0; r < kCommitCluster; ++r) a = better(a, *cluster.map_shared_rank(&cta_am, r));
-        row_am = a;
-    }
-    __syncthreads();
-    const float m = row_am.v;
-
-    // Pass 2: fixed-point confidence terms of the slice.
-    unsigned long long acc = 0;
-    if (ok) {
-        for (int e = tid * 4; e < cnt; e += kCommitThreads * 4) {
-            const float4 x = *reinterpret_cast<const float4*>(slice + e);
-            acc += fixed_term(__fsub_rn(x.x, m));
-            acc += fixed_term(__fsub_rn(x.y, m));
-            acc += fixed_term(__fsub_rn(x.z, m));
-            acc += fixed_term(__fsub_rn(x.w, m));
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) red_s[warp] = acc;
-    __syncthreads();
-    if (tid == 0) {
-        unsigned long long s = 0;
-        for (int w = 0; w < kCommitThreads / 32; ++w) s += red_s[w];
-        cta_sum = s;
-    }
-    cluster.sync();
-    if (rank == 0 && tid == 0) {
-        unsigned long long s = 0;
-        for (int r = 0; r < kCommitCluster; ++r) s += *cluster.map_shared_rank(&cta_sum, r);
-        p.key[row] = s;
-        p.arg[row] = row_am.i;
-    }
-    cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
-// One CTA per block: rank the still-masked rows by (key, row) and commit the
-// first k of them.
-__global__ void __launch_bounds__(1024) commit_select_kernel(const CommitParams p) {
-    extern __shared__ __align__(8) unsigned char sel_smem[];
-    unsigned long long* s_key = reinterpret_cast<unsigned long long*>(sel_smem);
-    uint8_t* s_m = sel_smem + static_cast<size_t>(p.L) * 8;
-    const int b = blockIdx.x;
+// Ranks the masked rows of block b by (key, row) and commits the first k.
+// Reads go through L2: the keys were written by other SMs.
+__device__ void select_block(const CommitParams& p, int b, unsigned long long* s_key,
+                             uint8_t* s_m) {
     const size_t base = static_cast<size_t>(b) * p.L;
     for (int i = threadIdx.x; i < p.L; i += blockDim.x) {
-        const uint8_t mk = p.masked[base + i];
+        const uint8_t mk = __ldcg(p.masked + base + i);
         s_m[i] = mk;
-        s_key[i] = mk ? p.key[base + i] : 0ull;
+        s_key[i] = mk ? __ldcg(p.key + base + i) : 0ull;
     }
     __syncthreads();  // every read of masked precedes any write of masked_out (they may alias)
     for (int i = threadIdx.x; i < p.L; i += blockDim.x) {
@@ -211,7 +121,7 @@ __global__ void __launch_bounds__(1024) commit_select_kernel(const CommitParams 
         for (int j = 0; j < p.L; ++j)
             rank += (s_m[j] && (s_key[j] < ki || (s_key[j] == ki && j < i))) ? 1 : 0;
         if (rank < p.k) {
-            p.tok[base + i] = p.arg[base + i];
+            p.tok[base + i] = __ldcg(p.arg + base + i);
             p.masked_out[base + i] = 0;
         } else {
             p.masked_out[base + i] = 1;
@@ -219,22 +129,162 @@ __global__ void __launch_bounds__(1024) commit_select_kernel(const CommitParams 
     }
 }
 
+__global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kCommitThreads)
+    commit_kernel(const CommitParams p) {
+    extern __shared__ __align__(128) unsigned char dyn[];
+    float* slice = reinterpret_cast<float*>(dyn);
+    __shared__ __align__(8) uint64_t bars[kPieces];
+    __shared__ ArgMax red_am[kCommitThreads / 32];
+    __shared__ unsigned long long red_s[kCommitThreads / 32];
+    __shared__ ArgMax cta_am;               // this CTA's (max, argmax), read by the cluster
+    __shared__ unsigned long long cta_sum;  // this CTA's partial key, read by rank 0
+    __shared__ ArgMax row_am;
+    __shared__ int is_last;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int row = blockIdx.x / kCommitCluster;
+    const int blk = row / p.L;
+    const unsigned rank = cluster.block_rank();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // uniform over the cluster: all its CTAs read the same flag
+    const bool masked = p.masked[row] != 0;
+
+    if (masked) {
+        const int v0 = static_cast<int>(rank) * p.slice;
+        const int cnt = max(0, min(p.slice, p.V - v0));  // multiple of 4
+        const float* src = p.logits + static_cast<size_t>(row) * p.V + v0;
+        const int per = (((cnt + kPieces - 1) / kPieces) + 3) & ~3;  // floats per piece
+
+        if (tid == 0) {
+            for (int i = 0; i < kPieces; ++i) mbar_init(&bars[i], 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            for (int i = 0; i < kPieces; ++i) {
+                const int lo = i * per, hi = min(cnt, lo + per);
+                if (hi > lo) {
+                    mbar_arrive_expect_tx(&bars[i], (hi - lo) * 4);
+                    bulk_load(slice + lo, src + lo, (hi - lo) * 4, &bars[i], pol);
+                }
+            }
+        }
+
+        // Pass 1: slice max, piece by piece as it lands; per thread the first
+        // float4 group that reaches its running max is remembered.
+        float best = -INFINITY;
+        int bestg = -1;
+        bool ok = true;
+        for (int i = 0; i < kPieces; ++i) {
+            const int lo = i * per, hi = min(cnt, lo + per);
+            if (hi <= lo) break;
+            if (!mbar_wait(&bars[i], 0, p.timeout_ns)) { ok = false; break; }
+            for (int e = lo + tid * 4; e < hi; e += kCommitThreads * 4) {
+                const float4 x = *reinterpret_cast<const float4*>(slice + e);
+                const float g = fmaxf(max3(x.x, x.y, x.z), x.w);
+                if (g > best) { best = g; bestg = e; }
+            }
+        }
+        if (!ok) {
+            if (tid == 0) atomicOr(p.status, kDevWaitTimeout);
+            // Let every copy already issued land before this CTA can exit.
+            for (int i = 0; i < kPieces; ++i)
+                if (min(cnt, i * per + per) > i * per) mbar_wait(&bars[i], 0, p.timeout_ns);
+        }
+        ArgMax am{-INFINITY, 0x7fffffff};
+        if (ok && bestg >= 0) {
+            const float4 x = *reinterpret_cast<const float4*>(slice + bestg);
+            const int j = x.x == best ? 0 : x.y == best ? 1 : x.z == best ? 2 : 3;
+            am = ArgMax{best, v0 + bestg + j};
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ArgMax other{__shfl_xor_sync(0xffffffffu, am.v, o),
+                         __shfl_xor_sync(0xffffffffu, am.i, o)};
+            am = better(am, other);
+        }
+        if (lane == 0) red_am[warp] = am;
+        __syncthreads();
+        if (tid == 0) {
+            ArgMax a = red_am[0];
+            for (int w = 1; w < kCommitThreads / 32; ++w) a = better(a, red_am[w]);
+            cta_am = a;
+        }
+        cluster.sync();
+        if (tid == 0) {
+            ArgMax a{-INFINITY, 0x7fffffff};
+            for (int r = 0; r < kCommitCluster; ++r)
+                a = better(a, *cluster.map_shared_rank(&cta_am, r));
+            row_am = a;
+        }
+        __syncthreads();
+        const float m = row_am.v;
+
+        // Pass 2: fixed-point confidence terms of the slice.
+        unsigned hi = 0;
+        int lo = 0;
+        if (ok) {
+            for (int e = tid * 4; e < cnt; e += kCommitThreads * 4) {
+                const float4 x = *reinterpret_cast<const float4*>(slice + e);
+                add_fixed_term(__fsub_rn(x.x, m), hi, lo);
+                add_fixed_term(__fsub_rn(x.y, m), hi, lo);
+                add_fixed_term(__fsub_rn(x.z, m), hi, lo);
+                add_fixed_term(__fsub_rn(x.w, m), hi, lo);
+            }
+        }
+        unsigned long long acc =
+            (static_cast<unsigned long long>(hi) << 20) + static_cast<long long>(lo);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) red_s[warp] = acc;
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long s = 0;
+            for (int w = 0; w < kCommitThreads / 32; ++w) s += red_s[w];
+            cta_sum = s;
+        }
+        cluster.sync();
+        if (rank == 0 && tid == 0) {
+            unsigned long long s = 0;
+            for (int r = 0; r < kCommitCluster; ++r) s += *cluster.map_shared_rank(&cta_sum, r);
+            p.key[row] = s;
+            p.arg[row] = row_am.i;
+        }
+        cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
+    }
+    if (rank != 0) return;
+
+    // Block ticket: the cluster of the block's last row to finish commits.
+    if (tid == 0) {
+        __threadfence();  // this row's key/arg before the ticket
+        const unsigned t = atomicInc(p.counters + blk, static_cast<unsigned>(p.L - 1));
+        is_last = t == static_cast<unsigned>(p.L - 1);  // the counter wrapped back to 0
+        __threadfence();
+    }
+    __syncthreads();
+    if (!is_last) return;
+    select_block(p, blk, reinterpret_cast<unsigned long long*>(dyn),
+                 dyn + static_cast<size_t>(p.L) * 8);
+}
+
 }  // namespace
 
+size_t commit_smem_bytes(int V, int L) {
+    const size_t slice = static_cast<size_t>((((V + kCommitCluster - 1) / kCommitCluster) + 3) & ~3) * 4;
+    const size_t sel = static_cast<size_t>(L) * 9;
+    return slice > sel ? slice : sel;
+}
+
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t s) {
-    const size_t rows_smem = static_cast<size_t>(p.slice) * 4;
-    commit_rows_kernel<<<static_cast<unsigned>(p.B * p.L) * kCommitCluster, kCommitThreads,
-                         rows_smem, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int threads = p.L >= 1024 ? 1024 : ((p.L + 31) / 32) * 32;
-    commit_select_kernel<<<p.B, threads, static_cast<size_t>(p.L) * 9, s>>>(p);
+    commit_kernel<<<static_cast<unsigned>(p.B * p.L) * kCommitCluster, kCommitThreads,
+                    commit_smem_bytes(p.V, p.L), s>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t configure_commit_kernels() {
-    return cudaFuncSetAttribute(commit_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kCommitSliceMax * 4);
+    return cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kCommitSmemMax);
 }
 
 }  // namespace tt

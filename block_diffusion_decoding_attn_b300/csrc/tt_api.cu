@@ -75,7 +75,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct AttnPlan {
-    int G, n_mtiles, nblk, nt_max, splits, chunk;
+    int G, n_mtiles, n_pairs, nblk, nt_max, splits, chunk;
     size_t ws_o_bytes, ws_bytes;
 };
 
@@ -101,9 +101,10 @@ int plan_attn(const tt_attn_desc* d, int num_sms, AttnPlan* pl) {
     if (d->num_splits < 0) return fail(TT_ERR_INVALID_ARG, "num_splits must be >= 0");
     pl->G = G;
     pl->n_mtiles = static_cast<int>((static_cast<long>(G) * d->L + tt::kTile - 1) / tt::kTile);
+    pl->n_pairs = (pl->n_mtiles + 1) / 2;
     pl->nblk = (d->L + tt::kTile - 1) / tt::kTile;
     pl->nt_max = (d->ctx_cap + tt::kTile - 1) / tt::kTile + pl->nblk;
-    const long units = static_cast<long>(d->B) * d->Hkv * pl->n_mtiles;
+    const long units = static_cast<long>(d->B) * d->Hkv * pl->n_pairs;
     int best = 1;
     if (d->num_splits > 0) {
         best = d->num_splits < pl->nt_max ? d->num_splits : pl->nt_max;
@@ -129,7 +130,7 @@ int plan_attn(const tt_attn_desc* d, int num_sms, AttnPlan* pl) {
     } else {
         pl->ws_o_bytes = pl->ws_bytes = 0;
     }
-    const long grid_x = static_cast<long>(pl->n_mtiles) * pl->splits;
+    const long grid_x = static_cast<long>(pl->n_pairs) * pl->splits;
     if (grid_x > 0x7fffffffL) return fail(TT_ERR_UNSUPPORTED, "grid too large");
     return TT_OK;
 }
@@ -291,7 +292,7 @@ int tt_block_attn(tt_handle h, const tt_attn_desc* d, const void* q, const void*
     }
     tt::AttnParams p;
     p.B = B; p.L = L; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.ctx_cap = d->ctx_cap;
-    p.n_mtiles = pl.n_mtiles; p.chunk = pl.chunk; p.nblk = pl.nblk;
+    p.n_mtiles = pl.n_mtiles; p.n_pairs = pl.n_pairs; p.chunk = pl.chunk; p.nblk = pl.nblk;
     const float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(D));
     p.scale_log2 = scale * 1.4426950408889634f;
     p.ctx_len = ctx_len;
@@ -314,7 +315,7 @@ int tt_block_attn(tt_handle h, const tt_attn_desc* d, const void* q, const void*
 size_t tt_commit_workspace_bytes(int B, int L) {
     if (B < 0 || L < 0) return 0;
     const size_t rows = static_cast<size_t>(B) * L;
-    return align256(rows * 8) + rows * 4;
+    return align256(rows * 8) + align256(rows * 4) + static_cast<size_t>(B) * 4;
 }
 
 int tt_commit(tt_handle h, const float* logits, int B, int L, int V, const uint8_t* masked, int k,
@@ -322,7 +323,8 @@ int tt_commit(tt_handle h, const float* logits, int B, int L, int V, const uint8
               void* stream) {
     if (!h) return fail(TT_ERR_INVALID_ARG, "tt_commit: handle is NULL");
     if (B < 0) return fail(TT_ERR_INVALID_ARG, "tt_commit: B=%d < 0", B);
-    if (L < 1 || L > 65536) return fail(TT_ERR_INVALID_ARG, "tt_commit: L=%d outside [1, 65536]", L);
+    if (L < 1 || L > tt::kCommitMaxL)
+        return fail(TT_ERR_UNSUPPORTED, "tt_commit: L=%d outside [1, %d]", L, tt::kCommitMaxL);
     if (k < 1) return fail(TT_ERR_INVALID_ARG, "tt_commit: k=%d < 1", k);
     if (V < 4 || V % 4 || V > tt::kCommitCluster * tt::kCommitSliceMax)
         return fail(TT_ERR_UNSUPPORTED, "tt_commit: V=%d must be a multiple of 4 in [4, %d]", V,
@@ -347,8 +349,10 @@ int tt_commit(tt_handle h, const float* logits, int B, int L, int V, const uint8
     p.tok = tok;
     p.masked_out = masked_out;
     p.key = static_cast<unsigned long long*>(workspace);
-    p.arg = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
-                                       align256(static_cast<size_t>(B) * L * 8));
+    const size_t rows = static_cast<size_t>(B) * L;
+    p.arg = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + align256(rows * 8));
+    p.counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + align256(rows * 8) +
+                                             align256(rows * 4));
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     cudaError_t e = tt::launch_commit(p, static_cast<cudaStream_t>(stream));

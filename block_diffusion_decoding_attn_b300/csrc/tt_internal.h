@@ -17,6 +17,7 @@ constexpr int kTile = 128;  // query rows per M tile and keys per KV tile
 struct AttnParams {
     int B, L, Hq, Hkv, G, ctx_cap;
     int n_mtiles;  // ceil(G*L / 128) query tiles per (b, kv head)
+    int n_pairs;   // ceil(n_mtiles / 2): a CTA takes two query tiles
     int chunk;     // KV tiles per split
     int nblk;      // ceil(L / 128) tiles of block keys
     float scale_log2;
@@ -48,6 +49,7 @@ struct CommitParams {
     uint8_t* masked_out;
     unsigned long long* key;  // [B*L]
     int32_t* arg;             // [B*L]
+    unsigned* counters;       // [B] block tickets; zero between calls
     unsigned* status;
     unsigned long long timeout_ns;
 };
@@ -55,7 +57,11 @@ struct CommitParams {
 constexpr int kCommitCluster = 8;       // CTAs sharing one logit row
 constexpr int kCommitThreads = 256;
 constexpr int kCommitSliceMax = 16384;  // fp32 logits per CTA (64 KB of shared memory)
+constexpr int kCommitMaxL = 16384;      // rows per block (the selection keeps 9 bytes/row in smem)
+constexpr int kCommitSmemMax = kCommitMaxL * 9 > kCommitSliceMax * 4 ? kCommitMaxL * 9
+                                                                      : kCommitSliceMax * 4;
 
+size_t commit_smem_bytes(int V, int L);
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t s);
 cudaError_t configure_commit_kernels();
 cudaError_t configure_attn_kernels();

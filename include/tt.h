@@ -136,9 +136,13 @@ int tt_block_attn(tt_handle handle, const tt_attn_desc* desc, const void* q, con
  *   tok        [B*L] int32, device, updated in place at committed rows
  *   masked_out [B*L] uint8, device; may be the same buffer as masked
  * Rows with masked[r] == 0 are not read. Supported: V % 4 == 0,
- * 4 <= V <= 131072, 1 <= L <= 65536, k >= 1 (k >= #masked commits all).
- * Workspace layout (after the call): uint64 key[B*L], then int32 arg[B*L],
- * valid at rows that were masked on entry.
+ * 4 <= V <= 131072, 1 <= L <= 16384, k >= 1 (k >= #masked commits all).
+ * Workspace (tt_commit_workspace_bytes, 256-byte aligned): uint64 key[B*L] at
+ * offset 0, int32 arg[B*L] at offset align256(8*B*L), uint32 ticket[B] at
+ * align256(8*B*L) + align256(4*B*L). key/arg hold, after the call, the key and
+ * prediction of every row that was masked on entry. The tickets must be ZERO
+ * before a workspace is first used (e.g. cudaMemset); every call leaves them
+ * zero again, so a workspace is zeroed once, not per call.
  * ------------------------------------------------------------------------ */
 size_t tt_commit_workspace_bytes(int B, int L);
 

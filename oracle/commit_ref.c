@@ -23,7 +23,8 @@
  *
  * The exponential (a reading: the page only says "confidence"):
  *   x < -30          -> q = 0  (2^40 * exp(-30) < 0.11 rounds to 0 anyway)
- *   t = RN32(x * LOG2E), n = round-half-even(t)
+ *   n = x * LOG2E rounded to the nearest integer, ties to even, from the exact
+ *       product: nb = fma(x, LOG2E, 1.5 * 2^23) (one rounding), n = nb - 1.5 * 2^23
  *   r = fma(-n, C1, x); r = fma(-n, C2, r)      (Cody and Waite reduction)
  *   p = c7; p = fma(p, r, c_j) for j = 6..0     (Taylor series, c_j = 1/j!)
  *   q = round-half-even(p * 2^(n+40))           (exact power-of-two scale)
@@ -44,11 +45,17 @@ static const float C1_F = (float)LN2_D;
 
 static float c2_f(void) { return (float)(LN2_D - (double)C1_F); }
 
+/* n = nearest integer (ties to even) to the exact product x * LOG2E; |n| < 2^22. */
+static float reduce_n(float x) {
+    const float magic = 12582912.0f; /* 1.5 * 2^23: sums in [2^23, 2^24) have ulp 1 */
+    const float nb = fmaf(x, LOG2E_F, magic);
+    return nb - magic;
+}
+
 /* e(x) for -30 <= x <= 0 as a float: p(r) * 2^n. Returns 0 below -30. */
 float tt_oracle_exp_own(float x) {
     if (x < -30.0f) return 0.0f;
-    const float t = x * LOG2E_F;
-    const float n = rintf(t); /* default rounding mode: to nearest, ties to even */
+    const float n = reduce_n(x);
     float r = fmaf(-n, C1_F, x);
     r = fmaf(-n, c2_f(), r);
     static const double inv_fact[8] = {1.0, 1.0, 1.0 / 2, 1.0 / 6, 1.0 / 24, 1.0 / 120, 1.0 / 720,
@@ -61,8 +68,7 @@ float tt_oracle_exp_own(float x) {
 /* q(x) = rint(2^40 * e(x)). */
 uint64_t tt_oracle_quant(float x) {
     if (x < -30.0f) return 0;
-    const float t = x * LOG2E_F;
-    const float n = rintf(t);
+    const float n = reduce_n(x);
     float r = fmaf(-n, C1_F, x);
     r = fmaf(-n, c2_f(), r);
     static const double inv_fact[8] = {1.0, 1.0, 1.0 / 2, 1.0 / 6, 1.0 / 24, 1.0 / 120, 1.0 / 720,

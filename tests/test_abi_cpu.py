@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(tt):
 
 def test_host_argument_errors(tt):
     lib = tt.lib()
-    assert lib.tt_commit_workspace_bytes(4, 32) == 1024 + 512
+    assert lib.tt_commit_workspace_bytes(4, 32) == 1024 + 512 + 16
     assert lib.tt_commit_workspace_bytes(-1, 3) == 0
     assert lib.tt_status_string(-2) == b"TT_ERR_UNSUPPORTED"
     # NULL handle is rejected before anything else
