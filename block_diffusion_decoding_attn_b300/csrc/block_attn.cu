@@ -300,10 +300,14 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int c = 0; c < kTile; ++c) s[c] = (c < kt.valid) ? s[c] : -INFINITY;
             }
-            float mx = s[0];
+            // row max: four independent chains of 3-input max, then combined
+            float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-            for (int c = 1; c + 1 < kTile; c += 2) mx = max3f(mx, s[c], s[c + 1]);
-            mx = fmaxf(mx, s[kTile - 1]);
+            for (int c = 4; c < kTile; c += 8) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) m4[q] = max3f(m4[q], s[c + 2 * q], s[c + 2 * q + 1]);
+            }
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             const float m_tile = mx * sl2;
             if (j == 0) {
                 m_run = m_tile;
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
             const float neg_m = -m_run;
-            float sum0 = 0.f, sum1 = 0.f;
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};  // 8 sum chains
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // P in two halves of 64 keys (32 columns each)
                 uint32_t pk[32];
@@ -334,15 +338,19 @@ __global__ void __launch_bounds__(320, 1)
                     float a0, a1;
                     fma2(a0, a1, s[h * 64 + c], s[h * 64 + c + 1], sl2, sl2, neg_m, neg_m);
                     const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
-                    add2(sum0, sum1, sum0, sum1, e0, e1);
+                    const int q = (c >> 1) & 3;
+                    add2(sa[q], sb[q], sa[q], sb[q], e0, e1);
                     pk[c >> 1] = pack_bf16x2(e0, e1);
                 }
                 tmem_st32(ts + h * 32, pk);  // P over the first 64 columns of S_X
             }
-            l_run += sum0 + sum1;
+            l_run += ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
             tc_fence_before();
             mbar_arrive(&p_full[x]);
         }
+        // The split merge (launched as a programmatic dependent) may start
+        // launching now; it still waits for this grid's completion.
+        if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_final[x], 0, limit));
         if (!ok) {
             if (lane == 0) atomicOr(p.status, kDevWaitTimeout);
@@ -396,6 +404,9 @@ __global__ void __launch_bounds__(320, 1)
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     constexpr int kPer = D / 32;  // columns per lane
+    // Launched as a programmatic dependent of the attention grid: wait until
+    // that grid has completed and its partials are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long gw = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const long rows_bk = static_cast<long>(p.G) * p.L;
@@ -472,12 +483,18 @@ cudaError_t launch_block_attn(const AttnMaps& maps, const AttnParams& p, int D, 
 
 cudaError_t launch_attn_merge(const AttnParams& p, int D, cudaStream_t s) {
     const long warps = static_cast<long>(p.G) * p.L * p.B * p.Hkv;
-    const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
-    if (D == 64)
-        attn_merge_kernel<64><<<blocks, 256, 0, s>>>(p);
-    else
-        attn_merge_kernel<128><<<blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((warps * 32 + 255) / 256), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return D == 64 ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, p)
+                   : cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, p);
 }
 
 }  // namespace tt

@@ -28,7 +28,8 @@
 // FP64 pipe, which is narrow on this part): the polynomial carries the 2^40
 // factor in its coefficients (exact power-of-two scaling), 2^n is added to the
 // exponent field, and rint splits into a multiple of 2^20 plus a remainder,
-// both read out of the bits of exact fp32 sums.
+// both read out of the bits of exact fp32 sums. The arithmetic runs on packed
+// f32x2 pairs (each half rounded exactly like the scalar operation).
 #include <cooperative_groups.h>
 
 #include "ptx.cuh"
@@ -56,30 +57,65 @@ constexpr float kMagic43 = 0x1.8p+43f;  // ... in [2^43, 2^44) have ulp 2^20
 constexpr int kMagic23Bits = 0x4B400000;
 constexpr int kMagic43Bits = 0x55400000;
 
-// Adds rint(2^40 * e(x)) for x <= 0 to the pair (hi, lo): term = hi * 2^20 + lo.
-// Explicit round-to-nearest intrinsics, so nothing is contracted differently.
-__device__ __forceinline__ void add_fixed_term(float x, unsigned& hi, int& lo) {
-    const float xc = fmaxf(x, -31.0f);  // terms below -30 are 0 either way
-    const float nb = __fmaf_rn(xc, kLog2e, kMagic23);  // 1.5*2^23 + n
-    const float n = __fsub_rn(nb, kMagic23);
-    float r = __fmaf_rn(-n, kLn2Hi, xc);
-    r = __fmaf_rn(-n, kLn2Lo, r);
-    float p = kC7;
-    p = __fmaf_rn(p, r, kC6);
-    p = __fmaf_rn(p, r, kC5);
-    p = __fmaf_rn(p, r, kC4);
-    p = __fmaf_rn(p, r, kC3);
-    p = __fmaf_rn(p, r, kC2);
-    p = __fmaf_rn(p, r, kC0);
-    p = __fmaf_rn(p, r, kC0);  // 2^40 * p(r), in [2^39.5, 2^40.5]
+// Packed fp32 pairs: one f32x2 instruction does the same round-to-nearest
+// operation on both halves, halving the issue slots of the term arithmetic.
+using f2 = unsigned long long;
+
+__device__ __forceinline__ f2 pk(float a, float b) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk(f2 r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ f2 dup(float c) { return pk(c, c); }
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+    f2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Adds rint(2^40 * e(x0)) + rint(2^40 * e(x1)) (x <= 0) to the pair
+// (hi, lo): sum of terms = hi * 2^20 + lo.
+__device__ __forceinline__ void add_fixed_terms(float x0, float x1, unsigned& hi, int& lo) {
+    const f2 x = pk(fmaxf(x0, -31.0f), fmaxf(x1, -31.0f));  // terms below -30 are 0 either way
+    const f2 nb = fma2(x, dup(kLog2e), dup(kMagic23));     // 1.5*2^23 + n
+    const f2 n = sub2(nb, dup(kMagic23));
+    f2 r = fma2(n, dup(-kLn2Hi), x);
+    r = fma2(n, dup(-kLn2Lo), r);
+    f2 p = fma2(dup(kC7), r, dup(kC6));
+    p = fma2(p, r, dup(kC5));
+    p = fma2(p, r, dup(kC4));
+    p = fma2(p, r, dup(kC3));
+    p = fma2(p, r, dup(kC2));
+    p = fma2(p, r, dup(kC0));
+    p = fma2(p, r, dup(kC0));  // 2^40 * p(r), in [2^39.5, 2^40.5]
+    float p0, p1, nb0, nb1;
+    upk(p, p0, p1);
+    upk(nb, nb0, nb1);
     // y = p * 2^n: add n to the exponent field; (bits(nb) << 23) == (n << 23) mod 2^32.
-    const float y = __int_as_float(__float_as_int(p) + (__float_as_int(nb) << 23));
-    const float a = __fadd_rn(y, kMagic43);  // 1.5*2^43 + 2^20 * round(y / 2^20)
-    const float yh = __fsub_rn(a, kMagic43);
-    const float rem = __fsub_rn(y, yh);       // exact, |rem| <= 2^19
-    const float b = __fadd_rn(rem, kMagic23);  // 1.5*2^23 + rint(rem)
-    hi += static_cast<unsigned>(__float_as_int(a) - kMagic43Bits);
-    lo += __float_as_int(b) - kMagic23Bits;
+    const f2 y = pk(__int_as_float(__float_as_int(p0) + (__float_as_int(nb0) << 23)),
+                    __int_as_float(__float_as_int(p1) + (__float_as_int(nb1) << 23)));
+    const f2 a = add2(y, dup(kMagic43));               // 1.5*2^43 + 2^20 * round(y / 2^20)
+    const f2 rem = sub2(y, sub2(a, dup(kMagic43)));    // exact, |rem| <= 2^19
+    const f2 b = add2(rem, dup(kMagic23));             // 1.5*2^23 + rint(rem)
+    float a0, a1, b0, b1;
+    upk(a, a0, a1);
+    upk(b, b0, b1);
+    hi += static_cast<unsigned>(__float_as_int(a0) - kMagic43Bits) +
+          static_cast<unsigned>(__float_as_int(a1) - kMagic43Bits);
+    lo += (__float_as_int(b0) - kMagic23Bits) + (__float_as_int(b1) - kMagic23Bits);
 }
 
 struct ArgMax {
@@ -227,10 +263,11 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kCommit
         if (ok) {
             for (int e = tid * 4; e < cnt; e += kCommitThreads * 4) {
                 const float4 x = *reinterpret_cast<const float4*>(slice + e);
-                add_fixed_term(__fsub_rn(x.x, m), hi, lo);
-                add_fixed_term(__fsub_rn(x.y, m), hi, lo);
-                add_fixed_term(__fsub_rn(x.z, m), hi, lo);
-                add_fixed_term(__fsub_rn(x.w, m), hi, lo);
+                float d0, d1, d2, d3;
+                upk(sub2(pk(x.x, x.y), dup(m)), d0, d1);
+                upk(sub2(pk(x.z, x.w), dup(m)), d2, d3);
+                add_fixed_terms(d0, d1, hi, lo);
+                add_fixed_terms(d2, d3, hi, lo);
             }
         }
         unsigned long long acc =
