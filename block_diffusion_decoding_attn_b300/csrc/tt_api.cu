@@ -149,6 +149,8 @@ int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const c
 
 }  // namespace
 
+void tt::record_host_error(const char* where, const char* msg) { fail(0, "%s: %s", where, msg); }
+
 extern "C" {
 
 const char* tt_status_string(int s) {

@@ -66,4 +66,7 @@ cudaError_t launch_commit(const CommitParams& p, cudaStream_t s);
 cudaError_t configure_commit_kernels();
 cudaError_t configure_attn_kernels();
 
+// Records "<where>: <msg>" as the calling thread's last host error (tt_last_error).
+void record_host_error(const char* where, const char* msg);
+
 }  // namespace tt

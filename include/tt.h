@@ -150,6 +150,29 @@ int tt_commit(tt_handle handle, const float* logits, int B, int L, int V, const 
               int k, int32_t* tok, uint8_t* masked_out, void* workspace, size_t workspace_bytes,
               void* stream);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free commit. The paper has no counterpart of this entry point:
+ * it is the same step as tt_commit, for callers that cannot allocate device
+ * memory -- a serving engine that reserves all of HBM for its own pool at
+ * start-up, or a plug-in host that forbids allocation while a request runs --
+ * and so can neither call cudaMalloc nor provide a zero-filled workspace.
+ *
+ * Arguments and results are those of tt_commit without the handle and the
+ * workspace; the scratch (per-row keys and predictions, per-block tickets)
+ * is a fixed 1 MiB array built into the library, present on every GPU that
+ * loads it until the process exits. Limits: B*L <= 65536 (larger sizes
+ * return TT_ERR_UNSUPPORTED with a message in tt_last_error), plus those of
+ * tt_commit. Works on the current CUDA device. The first call on a device
+ * sets that device up (looks up the array's device address, sets kernel
+ * attributes); make that first call before any stream capture. Each call
+ * clears the tickets on `stream` (cudaMemsetAsync) and allocates nothing.
+ * All calls share the one array: calls whose GPU work overlaps (other
+ * streams, other threads) race and must be ordered by the caller. Device-side
+ * wait timeouts are not reported (there is no handle status word).
+ * ------------------------------------------------------------------------ */
+int tt_commit_noalloc(const float* logits, int B, int L, int V, const uint8_t* masked, int k,
+                      int32_t* tok, uint8_t* masked_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
