@@ -1,21 +1,41 @@
 // Unmask/commit step of the TwoTower sampler ("Nemotron-Labs-TwoTower",
 // Section 2.2, Algorithm 2, confidence unmasking) with a fixed budget of k
-// commits per block per step. One launch:
+// commits per block per step. One launch.
 //
-// One 8-CTA cluster per row: each CTA bulk-copies its 1/8 slice of the fp32
-// logit row into shared memory (TMA, evict-first) and finds the slice's max
-// and first argmax; the cluster agrees on the row maximum m through
-// distributed shared memory; each CTA then sums the canonical fixed-point
-// terms q(l_v - m) of its slice from shared memory and CTA 0 adds the eight
-// partial sums:
-//     key[r] = sum_v rint(2^40 * e(RN32(l_v - m))),  arg[r] = first argmax
-// The sum is an integer, so the key does not depend on the reduction order and
-// matches a scalar CPU loop bit for bit. key / 2^40 = 1 / (max softmax
-// probability) up to the rounding of e; smaller key = more confident.
-// Every row's cluster then takes a ticket for its block; the cluster that
-// takes the last ticket ranks the block's masked rows by (key, row) and
-// commits the first min(k, #masked): tok[r] = arg[r], masked_out[r] = 0.
+// For every still-masked row r:
+//     m = max_v l_v,  arg[r] = lowest v with l_v == m (greedy prediction)
+//     key[r] = sum_v rint(2^40 * e(RN32(l_v - m)))
+// The key is an integer, so it does not depend on the reduction order and
+// matches a scalar CPU loop bit for bit; key / 2^40 = 1 / (max softmax
+// probability) up to the rounding of e, so a smaller key is more confident.
+// When every row of a block is done, the block's masked rows are ranked by
+// (key, row) and the first min(k, #masked) are committed: tok[r] = arg[r],
+// masked_out[r] = 0.
 //
+// Layout of the work: a persistent grid of 4-CTA clusters. Cluster c owns the
+// rows r = c, c + #clusters, ...; CTA j of the cluster owns the j-th quarter
+// of every row (128 KB at V = 131072). Per CTA:
+//   warp 16 (producer): for each owned masked row, bulk TMA copies of the
+//       CTA's quarter in 64 KB chunks into a 3-slot shared-memory ring (L2
+//       evict-first); unmasked rows are only marked in masked_out;
+//   warps 0-15 (consumers, two groups of 8 warps taking alternate rows): per
+//       row the group
+//       pass 1  streams the chunks from shared memory into its half of the
+//               tensor memory (TMEM: 128 lanes x 256 columns = one quarter row),
+//               taking the slice max / first argmax on the way and freeing each
+//               slot at once; the result goes to all 4 CTAs (DSMEM store +
+//               remote mbarrier arrive; no cluster-wide barrier)
+//       wait    for the 4 slice results   -> row max m and prediction
+//       pass 2  reads the slice back from TMEM, 32 columns at a time, and sums
+//               its fixed-point terms -> partial key sent to CTA 0;
+//       while one group waits for the cluster, the other computes, and the
+//       ring keeps streaming;
+//   warp 17 of CTA 0 (collector): adds each row's 4 partial keys, writes
+//       key/arg; per block it takes one ticket for all of the cluster's rows
+//       of the block (the count is the block's number of masked rows); the
+//       warp that completes the count ranks the block's masked rows and
+//       commits.
+
 // e(x) is an fp32 exponential defined for this purpose (Cody and Waite range
 // reduction, then the degree-7 Taylor polynomial of exp, all with
 // round-to-nearest fused multiply-adds):
@@ -30,12 +50,8 @@
 // exponent field, and rint splits into a multiple of 2^20 plus a remainder,
 // both read out of the bits of exact fp32 sums. The arithmetic runs on packed
 // f32x2 pairs (each half rounded exactly like the scalar operation).
-#include <cooperative_groups.h>
-
 #include "ptx.cuh"
 #include "tt_internal.h"
-
-namespace cg = cooperative_groups;
 
 namespace tt {
 
@@ -54,8 +70,23 @@ constexpr float kC6 = 0x1.6c16c2p+30f;
 constexpr float kC7 = 0x1.a01a02p+27f;
 constexpr float kMagic23 = 0x1.8p+23f;  // fp32 sums in [2^23, 2^24) have ulp 1
 constexpr float kMagic43 = 0x1.8p+43f;  // ... in [2^43, 2^44) have ulp 2^20
-constexpr int kMagic23Bits = 0x4B400000;
-constexpr int kMagic43Bits = 0x55400000;
+constexpr unsigned kMagic23Bits = 0x4B400000u;
+constexpr unsigned kMagic43Bits = 0x55400000u;
+
+constexpr int kSlots = 3;                 // ring depth: 64 KB chunks landing per CTA
+constexpr int kChunk = 16384;             // logits per ring slot
+constexpr int kGroupThreads = 256;        // one consumer group: 8 warps
+constexpr int kGroups = 2;                // consumer groups, alternate rows
+constexpr int kConsumers = kGroups * kGroupThreads;
+constexpr int kProducerWarp = kConsumers / 32;      // warp 16
+constexpr int kCollectorWarp = kProducerWarp + 1;   // warp 17 (CTA 0 only)
+constexpr int kThreads = kConsumers + 64;
+constexpr int kSliceMax = 2 * kChunk;               // 32768 logits per CTA
+constexpr int kColsPerThread = kSliceMax / kGroupThreads * 2 / 2;  // 128 TMEM columns
+constexpr int kXchg = 8;                  // exchange slots (rows in flight in the cluster)
+constexpr int kSelChunk = 2048;           // keys staged per selection pass
+static_assert(kSliceMax == kCommitSliceMax, "slice per CTA");
+static_assert(kColsPerThread == 128, "two groups x two column halves x 128 = 512 TMEM columns");
 
 // Packed fp32 pairs: one f32x2 instruction does the same round-to-nearest
 // operation on both halves, halving the issue slots of the term arithmetic.
@@ -70,65 +101,71 @@ __device__ __forceinline__ void upk(f2 r, float& a, float& b) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
 }
 __device__ __forceinline__ f2 dup(float c) { return pk(c, c); }
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+__device__ __forceinline__ f2 ffma2(f2 a, f2 b, f2 c) {
     f2 d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
-__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+__device__ __forceinline__ f2 fadd2(f2 a, f2 b) {
     f2 d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+__device__ __forceinline__ f2 fsub2(f2 a, f2 b) {
     f2 d;
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 
-// Adds rint(2^40 * e(x0)) + rint(2^40 * e(x1)) (x <= 0) to the pair
-// (hi, lo): sum of terms = hi * 2^20 + lo.
-__device__ __forceinline__ void add_fixed_terms(float x0, float x1, unsigned& hi, int& lo) {
-    const f2 x = pk(fmaxf(x0, -31.0f), fmaxf(x1, -31.0f));  // terms below -30 are 0 either way
-    const f2 nb = fma2(x, dup(kLog2e), dup(kMagic23));     // 1.5*2^23 + n
-    const f2 n = sub2(nb, dup(kMagic23));
-    f2 r = fma2(n, dup(-kLn2Hi), x);
-    r = fma2(n, dup(-kLn2Lo), r);
-    f2 p = fma2(dup(kC7), r, dup(kC6));
-    p = fma2(p, r, dup(kC5));
-    p = fma2(p, r, dup(kC4));
-    p = fma2(p, r, dup(kC3));
-    p = fma2(p, r, dup(kC2));
-    p = fma2(p, r, dup(kC0));
-    p = fma2(p, r, dup(kC0));  // 2^40 * p(r), in [2^39.5, 2^40.5]
+// Adds the fixed-point terms of x0, x1 (RN32(l - m) clamped below at -31;
+// terms below -28.4 round to 0 either way) to the accumulators:
+//   sum of terms = (hi - cnt * kMagic43Bits) * 2^20 + (lo - cnt * kMagic23Bits)
+// (mod 2^32 each), with cnt the number of terms added; the constant offsets
+// are taken out once at the end.
+__device__ __forceinline__ void add_terms(f2 x, unsigned& hi, unsigned& lo) {
+    const f2 nb = ffma2(x, dup(kLog2e), dup(kMagic23));  // 1.5*2^23 + n
+    const f2 n = fsub2(nb, dup(kMagic23));
+    f2 r = ffma2(n, dup(-kLn2Hi), x);
+    r = ffma2(n, dup(-kLn2Lo), r);
+    f2 p = ffma2(dup(kC7), r, dup(kC6));
+    p = ffma2(p, r, dup(kC5));
+    p = ffma2(p, r, dup(kC4));
+    p = ffma2(p, r, dup(kC3));
+    p = ffma2(p, r, dup(kC2));
+    p = ffma2(p, r, dup(kC0));
+    p = ffma2(p, r, dup(kC0));  // 2^40 * p(r), in [2^39.5, 2^40.5]
     float p0, p1, nb0, nb1;
     upk(p, p0, p1);
     upk(nb, nb0, nb1);
     // y = p * 2^n: add n to the exponent field; (bits(nb) << 23) == (n << 23) mod 2^32.
-    const f2 y = pk(__int_as_float(__float_as_int(p0) + (__float_as_int(nb0) << 23)),
-                    __int_as_float(__float_as_int(p1) + (__float_as_int(nb1) << 23)));
-    const f2 a = add2(y, dup(kMagic43));               // 1.5*2^43 + 2^20 * round(y / 2^20)
-    const f2 rem = sub2(y, sub2(a, dup(kMagic43)));    // exact, |rem| <= 2^19
-    const f2 b = add2(rem, dup(kMagic23));             // 1.5*2^23 + rint(rem)
+    const f2 y = pk(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(nb0) << 23)),
+                    __uint_as_float(__float_as_uint(p1) + (__float_as_uint(nb1) << 23)));
+    const f2 a = fadd2(y, dup(kMagic43));               // 1.5*2^43 + 2^20 * round(y / 2^20)
+    const f2 rem = fsub2(y, fsub2(a, dup(kMagic43)));   // exact, |rem| <= 2^19
+    const f2 b = fadd2(rem, dup(kMagic23));             // 1.5*2^23 + rint(rem)
     float a0, a1, b0, b1;
     upk(a, a0, a1);
     upk(b, b0, b1);
-    hi += static_cast<unsigned>(__float_as_int(a0) - kMagic43Bits) +
-          static_cast<unsigned>(__float_as_int(a1) - kMagic43Bits);
-    lo += (__float_as_int(b0) - kMagic23Bits) + (__float_as_int(b1) - kMagic23Bits);
+    hi += __float_as_uint(a0) + __float_as_uint(a1);
+    lo += __float_as_uint(b0) + __float_as_uint(b1);
 }
 
-struct ArgMax {
-    float v;
-    int i;
-};
-
-// Larger value wins; equal values -> lower index (first occurrence).
-__device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
-    return (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;
+// (value, index) as one orderable 64-bit word: a larger value wins, equal
+// values go to the lower index. -0.0 is folded into +0.0 first (they compare
+// equal). 0 is below every encoded pair.
+__device__ __forceinline__ unsigned long long enc_argmax(float v, int i) {
+    unsigned u = __float_as_uint(v + 0.0f);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - static_cast<unsigned>(i));
 }
-
-constexpr int kPieces = 4;  // bulk copies per slice, each with its own barrier
+__device__ __forceinline__ float dec_value(unsigned long long e) {
+    unsigned u = static_cast<unsigned>(e >> 32);
+    u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+    return __uint_as_float(u);
+}
+__device__ __forceinline__ int dec_index(unsigned long long e) {
+    return static_cast<int>(0xFFFFFFFFu - static_cast<unsigned>(e));
+}
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
@@ -136,192 +173,461 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
-// Ranks the masked rows of block b by (key, row) and commits the first k.
-// Reads go through L2: the keys were written by other SMs.
-__device__ void select_block(const CommitParams& p, int b, unsigned long long* s_key,
-                             uint8_t* s_m) {
-    const size_t base = static_cast<size_t>(b) * p.L;
-    for (int i = threadIdx.x; i < p.L; i += blockDim.x) {
-        const uint8_t mk = __ldcg(p.masked + base + i);
-        s_m[i] = mk;
-        s_key[i] = mk ? __ldcg(p.key + base + i) : 0ull;
-    }
-    __syncthreads();  // every read of masked precedes any write of masked_out (they may alias)
-    for (int i = threadIdx.x; i < p.L; i += blockDim.x) {
-        if (!s_m[i]) {
-            p.masked_out[base + i] = 0;
-            continue;
-        }
-        const unsigned long long ki = s_key[i];
-        int rank = 0;
-        for (int j = 0; j < p.L; ++j)
-            rank += (s_m[j] && (s_key[j] < ki || (s_key[j] == ki && j < i))) ? 1 : 0;
-        if (rank < p.k) {
-            p.tok[base + i] = __ldcg(p.arg + base + i);
-            p.masked_out[base + i] = 0;
-        } else {
-            p.masked_out[base + i] = 1;
-        }
-    }
+__device__ __forceinline__ unsigned long long shfl_xor64(unsigned long long v, int o) {
+    return __shfl_xor_sync(0xffffffffu, v, o);
 }
 
-__global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kCommitThreads)
-    commit_kernel(const CommitParams p) {
-    extern __shared__ __align__(128) unsigned char dyn[];
-    float* slice = reinterpret_cast<float*>(dyn);
-    __shared__ __align__(8) uint64_t bars[kPieces];
-    __shared__ ArgMax red_am[kCommitThreads / 32];
-    __shared__ unsigned long long red_s[kCommitThreads / 32];
-    __shared__ ArgMax cta_am;               // this CTA's (max, argmax), read by the cluster
-    __shared__ unsigned long long cta_sum;  // this CTA's partial key, read by rank 0
-    __shared__ ArgMax row_am;
-    __shared__ int is_last;
+struct CommitShared {
+    uint64_t full[kSlots];      // producer -> consumers: chunk landed
+    uint64_t empty[kSlots];     // consumers -> producer: slot free (8 warp arrivals)
+    uint64_t am_bar[kXchg];     // one arrival per CTA: its slice (max, argmax)
+    uint64_t sum_bar[kXchg];    // one arrival per CTA at CTA 0: its partial key
+    uint64_t col_done[kXchg];   // CTA 0: the collector has finished the row
+    unsigned long long am_in[kXchg][kCommitCluster];   // written by the cluster's CTAs
+    unsigned long long sum_in[kXchg][kCommitCluster];  // (CTA 0 only)
+    int col_arg[kXchg];                                 // (CTA 0) prediction of the row
+    unsigned long long red_am[kGroups][kGroupThreads / 32];
+    unsigned long long red_sum[kGroups][kGroupThreads / 32];
+    int total;              // masked rows of this cluster
+    uint32_t tmem;          // TMEM base address (512 columns)
+};
 
-    cg::cluster_group cluster = cg::this_cluster();
-    const int row = blockIdx.x / kCommitCluster;
-    const int blk = row / p.L;
-    const unsigned rank = cluster.block_rank();
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // uniform over the cluster: all its CTAs read the same flag
-    const bool masked = p.masked[row] != 0;
-
-    if (masked) {
-        const int v0 = static_cast<int>(rank) * p.slice;
-        const int cnt = max(0, min(p.slice, p.V - v0));  // multiple of 4
-        const float* src = p.logits + static_cast<size_t>(row) * p.V + v0;
-        const int per = (((cnt + kPieces - 1) / kPieces) + 3) & ~3;  // floats per piece
-
-        if (tid == 0) {
-            for (int i = 0; i < kPieces; ++i) mbar_init(&bars[i], 1);
-            fence_mbar_init();
+// Commits the k most confident masked rows of block b: tok[r] = arg[r],
+// masked_out[r] = 0; the block's other masked rows get masked_out[r] = 1
+// (unmasked rows are written by the row's owner). Order: (key, row)
+// ascending. Every masked row of the block has written its key and
+// prediction (the block's last ticket was taken); reads go through L2. Run by
+// one warp. All masked flags are read before any write, since masked_out may
+// alias masked. n = number of masked rows in the block.
+//   n <= k: every masked row commits, no ranking;
+//   L <= kSelChunk: k rounds of a warp argmin over the keys staged in shared
+//       memory, each round taking the smallest (key, row) above the last;
+//   larger L: each row's rank is counted over the keys, chunk by chunk.
+__device__ void select_block(const CommitParams& p, int b, int n, unsigned long long* s_key,
+                             uint32_t* s_mbits, uint32_t* s_cbits, int lane) {
+    const size_t base = static_cast<size_t>(b) * p.L;
+    const int nw = (p.L + 31) / 32;
+    for (int w = 0; w < nw; ++w) {
+        const int i = w * 32 + lane;
+        const bool mi = i < p.L && __ldcg(p.masked + base + i) != 0;
+        const uint32_t mb = __ballot_sync(0xffffffffu, mi);
+        if (lane == 0) {
+            s_mbits[w] = mb;
+            s_cbits[w] = n <= p.k ? mb : 0u;
         }
-        __syncthreads();
-        if (tid == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            for (int i = 0; i < kPieces; ++i) {
-                const int lo = i * per, hi = min(cnt, lo + per);
-                if (hi > lo) {
-                    mbar_arrive_expect_tx(&bars[i], (hi - lo) * 4);
-                    bulk_load(slice + lo, src + lo, (hi - lo) * 4, &bars[i], pol);
+    }
+    __syncwarp();
+    if (n > p.k && p.L <= kSelChunk) {
+        for (int j = lane; j < p.L; j += 32)
+            s_key[j] = (s_mbits[j >> 5] >> (j & 31)) & 1u ? __ldcg(p.key + base + j) : ~0ull;
+        __syncwarp();
+        unsigned long long lk = 0;  // last chosen (key, row); row -1: none yet
+        int lr = -1;
+        for (int round = 0; round < p.k; ++round) {
+            unsigned long long bk = ~0ull;
+            int br = 0x7fffffff;
+            for (int j = lane; j < p.L; j += 32) {
+                const unsigned long long kj = s_key[j];
+                const bool above = kj > lk || (kj == lk && j > lr);
+                const bool below = kj < bk || (kj == bk && j < br);
+                if (kj != ~0ull && above && below) { bk = kj; br = j; }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long ok_ = __shfl_xor_sync(0xffffffffu, bk, o);
+                const int orow = __shfl_xor_sync(0xffffffffu, br, o);
+                if (ok_ < bk || (ok_ == bk && orow < br)) { bk = ok_; br = orow; }
+            }
+            if (br == 0x7fffffff) break;
+            if (lane == 0) s_cbits[br >> 5] |= 1u << (br & 31);
+            lk = bk;
+            lr = br;
+        }
+    } else if (n > p.k) {
+        for (int w = 0; w < nw; ++w) {
+            const int i = w * 32 + lane;
+            const bool mi = (s_mbits[w] >> lane) & 1u;
+            const unsigned long long ki = mi ? __ldcg(p.key + base + i) : 0ull;
+            int rank = 0;
+            for (int j0 = 0; j0 < p.L; j0 += kSelChunk) {
+                const int cn = min(kSelChunk, p.L - j0);
+                __syncwarp();
+                for (int j = lane; j < cn; j += 32)
+                    s_key[j] = (s_mbits[(j0 + j) >> 5] >> ((j0 + j) & 31)) & 1u
+                                   ? __ldcg(p.key + base + j0 + j)
+                                   : ~0ull;
+                __syncwarp();
+                const int lim = i - j0;  // rows j0 + j < i win ties
+                for (int j = 0; j < cn; ++j) {
+                    const unsigned long long kj = s_key[j];
+                    rank += (kj < ki || (kj == ki && j < lim)) ? 1 : 0;
                 }
             }
+            const uint32_t cb = __ballot_sync(0xffffffffu, mi && rank < p.k);
+            if (lane == 0) s_cbits[w] = cb;
         }
-
-        // Pass 1: slice max, piece by piece as it lands; per thread the first
-        // float4 group that reaches its running max is remembered.
-        float best = -INFINITY;
-        int bestg = -1;
-        bool ok = true;
-        for (int i = 0; i < kPieces; ++i) {
-            const int lo = i * per, hi = min(cnt, lo + per);
-            if (hi <= lo) break;
-            if (!mbar_wait(&bars[i], 0, p.timeout_ns)) { ok = false; break; }
-            for (int e = lo + tid * 4; e < hi; e += kCommitThreads * 4) {
-                const float4 x = *reinterpret_cast<const float4*>(slice + e);
-                const float g = fmaxf(max3(x.x, x.y, x.z), x.w);
-                if (g > best) { best = g; bestg = e; }
-            }
-        }
-        if (!ok) {
-            if (tid == 0) atomicOr(p.status, kDevWaitTimeout);
-            // Let every copy already issued land before this CTA can exit.
-            for (int i = 0; i < kPieces; ++i)
-                if (min(cnt, i * per + per) > i * per) mbar_wait(&bars[i], 0, p.timeout_ns);
-        }
-        ArgMax am{-INFINITY, 0x7fffffff};
-        if (ok && bestg >= 0) {
-            const float4 x = *reinterpret_cast<const float4*>(slice + bestg);
-            const int j = x.x == best ? 0 : x.y == best ? 1 : x.z == best ? 2 : 3;
-            am = ArgMax{best, v0 + bestg + j};
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            ArgMax other{__shfl_xor_sync(0xffffffffu, am.v, o),
-                         __shfl_xor_sync(0xffffffffu, am.i, o)};
-            am = better(am, other);
-        }
-        if (lane == 0) red_am[warp] = am;
-        __syncthreads();
-        if (tid == 0) {
-            ArgMax a = red_am[0];
-            for (int w = 1; w < kCommitThreads / 32; ++w) a = better(a, red_am[w]);
-            cta_am = a;
-        }
-        cluster.sync();
-        if (tid == 0) {
-            ArgMax a{-INFINITY, 0x7fffffff};
-            for (int r = 0; r < kCommitCluster; ++r)
-                a = better(a, *cluster.map_shared_rank(&cta_am, r));
-            row_am = a;
-        }
-        __syncthreads();
-        const float m = row_am.v;
-
-        // Pass 2: fixed-point confidence terms of the slice.
-        unsigned hi = 0;
-        int lo = 0;
-        if (ok) {
-            for (int e = tid * 4; e < cnt; e += kCommitThreads * 4) {
-                const float4 x = *reinterpret_cast<const float4*>(slice + e);
-                float d0, d1, d2, d3;
-                upk(sub2(pk(x.x, x.y), dup(m)), d0, d1);
-                upk(sub2(pk(x.z, x.w), dup(m)), d2, d3);
-                add_fixed_terms(d0, d1, hi, lo);
-                add_fixed_terms(d2, d3, hi, lo);
-            }
-        }
-        unsigned long long acc =
-            (static_cast<unsigned long long>(hi) << 20) + static_cast<long long>(lo);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) red_s[warp] = acc;
-        __syncthreads();
-        if (tid == 0) {
-            unsigned long long s = 0;
-            for (int w = 0; w < kCommitThreads / 32; ++w) s += red_s[w];
-            cta_sum = s;
-        }
-        cluster.sync();
-        if (rank == 0 && tid == 0) {
-            unsigned long long s = 0;
-            for (int r = 0; r < kCommitCluster; ++r) s += *cluster.map_shared_rank(&cta_sum, r);
-            p.key[row] = s;
-            p.arg[row] = row_am.i;
-        }
-        cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
     }
-    if (rank != 0) return;
+    __syncwarp();
+    for (int w = 0; w < nw; ++w) {
+        const int i = w * 32 + lane;
+        if ((s_mbits[w] >> lane) & 1u) {
+            const bool c = (s_cbits[w] >> lane) & 1u;
+            if (c) p.tok[base + i] = __ldcg(p.arg + base + i);
+            p.masked_out[base + i] = c ? 0 : 1;
+        }
+    }
+    __syncwarp();
+}
 
-    // Block ticket: the cluster of the block's last row to finish commits.
+// Masked rows of block b (read by one warp).
+__device__ int count_masked(const CommitParams& p, int b, int lane) {
+    const uint8_t* m = p.masked + static_cast<size_t>(b) * p.L;
+    int c = 0;
+    for (int i = lane; i < p.L; i += 32) c += __ldcg(m + i) != 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    return c;
+}
+
+__global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThreads, 1)
+    commit_kernel(const CommitParams p) {
+    extern __shared__ __align__(128) unsigned char dyn[];
+    __shared__ CommitShared sh;
+    float* ring = reinterpret_cast<float*>(dyn);
+    unsigned char* sel_base = dyn + static_cast<size_t>(kSlots) * kChunk * 4;
+    unsigned long long* s_key = reinterpret_cast<unsigned long long*>(sel_base);
+    uint32_t* s_mbits = reinterpret_cast<uint32_t*>(sel_base + kSelChunk * 8);
+    uint32_t* s_cbits = s_mbits + kCommitMaxL / 32;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cid = static_cast<int>(cluster_id_x());
+    const int ncl = static_cast<int>(nclusters_x());
+    const int rows = p.B * p.L;
+    const int v0 = static_cast<int>(rank) * p.slice;
+    const int cnt = max(0, min(p.slice, p.V - v0));  // this CTA's logits per row (multiple of 4)
+    const int nchunks = (cnt + kChunk - 1) / kChunk;  // ring entries per row (0 if cnt == 0)
+    const uint64_t limit = p.timeout_ns;
+
     if (tid == 0) {
-        __threadfence();  // this row's key/arg before the ticket
-        const unsigned t = atomicInc(p.counters + blk, static_cast<unsigned>(p.L - 1));
-        is_last = t == static_cast<unsigned>(p.L - 1);  // the counter wrapped back to 0
-        __threadfence();
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], kGroupThreads / 32);
+        }
+        for (int q = 0; q < kXchg; ++q) {
+            mbar_init(&sh.am_bar[q], kCommitCluster);
+            mbar_init(&sh.sum_bar[q], kCommitCluster);
+            mbar_init(&sh.col_done[q], 1);
+        }
+        fence_mbar_init();
     }
-    __syncthreads();
-    if (!is_last) return;
-    select_block(p, blk, reinterpret_cast<unsigned long long*>(dyn),
-                 dyn + static_cast<size_t>(p.L) * 8);
+    if (warp == 0) {
+        tmem_alloc(&sh.tmem, 512);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp) {  // the cluster's masked rows (every role loops to this count)
+        int c = 0;
+        for (int r = cid + lane * ncl; r < rows; r += 32 * ncl) c += __ldcg(p.masked + r) != 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        if (lane == 0) sh.total = c;
+    }
+    tc_fence_before();
+    // Every CTA's barriers are initialised before any remote arrival.
+    cluster_sync_all();
+    tc_fence_after();
+
+    if (warp == kProducerWarp) {
+        // ---------------------------------------------------------------- producer
+        // The masked rows of this cluster go through the ring in row order,
+        // max(nchunks, 1) entries each; the unmasked ones are only marked in
+        // masked_out.
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            const int per_row = max(nchunks, 1);
+            int it = 0;  // ring entries issued
+            bool ok = true;
+            for (int r = cid; r < rows && ok; r += ncl) {
+                // masked may alias masked_out: this read precedes the block's
+                // selection, which waits for this row's ticket.
+                if (__ldcg(p.masked + r) == 0) {
+                    if (rank == 0) p.masked_out[r] = 0;
+                    continue;
+                }
+                for (int c = 0; c < per_row; ++c, ++it) {
+                    const int s = it % kSlots;
+                    if (it >= kSlots && !mbar_wait(&sh.empty[s], ((it / kSlots) - 1) & 1, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const int lo = c * kChunk, n = min(kChunk, cnt - lo);
+                    if (n > 0) {
+                        mbar_arrive_expect_tx(&sh.full[s], static_cast<uint32_t>(n) * 4);
+                        bulk_load(ring + static_cast<size_t>(s) * kChunk,
+                                  p.logits + static_cast<size_t>(r) * p.V + v0 + lo,
+                                  static_cast<uint32_t>(n) * 4, &sh.full[s], pol);
+                    } else {
+                        mbar_arrive(&sh.full[s]);
+                    }
+                }
+            }
+            if (!ok) {
+                atomicOr(p.status, kDevWaitTimeout);
+                // Let the copies already issued land before the CTA can exit.
+                for (int j = it - kSlots < 0 ? 0 : it - kSlots; j < it; ++j)
+                    mbar_wait(&sh.full[j % kSlots], (j / kSlots) & 1, limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kCollectorWarp) {
+        // ---------------------------------------------------------------- collector
+        // CTA 0: adds each row's partial keys and writes key / prediction.
+        // The cluster's rows of one block are consecutive in its row order;
+        // once they are all written, it adds their number to the block's
+        // ticket counter, and the cluster that completes the count (the
+        // block's number of masked rows) selects the block.
+        if (rank == 0) {
+            int it = 0, cb = -1, cnum = 0, cmine = 0;
+            bool ok = true;
+            auto flush = [&]() {
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence();  // the rows' key / arg before the ticket
+                    const unsigned t = atomicAdd(p.counters + cb, static_cast<unsigned>(cmine));
+                    last = t + static_cast<unsigned>(cmine) == static_cast<unsigned>(cnum);
+                    if (last) {
+                        p.counters[cb] = 0;  // no other ticket of this call remains
+                        __threadfence();
+                    }
+                }
+                if (__shfl_sync(0xffffffffu, last, 0))
+                    select_block(p, cb, cnum, s_key, s_mbits, s_cbits, lane);
+            };
+            for (int r = cid; r < rows; r += ncl) {
+                if (__ldcg(p.masked + r) == 0) continue;
+                const int q = it % kXchg;
+                if (!mbar_wait_cluster(&sh.sum_bar[q], (it / kXchg) & 1, limit)) {
+                    ok = false;
+                    break;
+                }
+                unsigned long long key = 0;
+#pragma unroll
+                for (int j = 0; j < kCommitCluster; ++j) key += sh.sum_in[q][j];
+                const int arg = sh.col_arg[q];
+                __syncwarp();
+                if (lane == 0) {
+                    p.key[r] = key;
+                    p.arg[r] = arg;
+                    mbar_arrive(&sh.col_done[q]);
+                }
+                ++it;
+                const int b = r / p.L;
+                if (b != cb) {
+                    if (cb >= 0) flush();
+                    cb = b;
+                    cmine = 0;
+                    cnum = count_masked(p, b, lane);
+                }
+                ++cmine;
+            }
+            if (ok && cb >= 0) flush();
+            if (!ok && lane == 0) atomicOr(p.status, kDevWaitTimeout);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- consumers
+        // Group g takes rows g, g + 2, ... of the cluster's sequence. Every
+        // named barrier of the group also ANDs the threads' wait results, so
+        // a wait that gave up in any thread ends the group's loop in all of
+        // them at the same barrier.
+        const int g = warp / (kGroupThreads / 32);
+        const int gw = warp % (kGroupThreads / 32);
+        const int gt = tid % kGroupThreads;
+        const uint32_t bar_id = 1 + g;
+        // This thread's TMEM: lane 32 * (warp % 4) + lane, 128 columns from
+        // 256 g + 128 (gw / 4). Chunk c of the slice lands in columns
+        // 64 c .. 64 c + 63 of them: float4 u of the chunk (slice element
+        // c * kChunk + 4 * (u * 256 + gt)) in columns 64 c + 4 u .. + 3, so
+        // the columns run in slice order for every thread.
+        const uint32_t tbase = sh.tmem + ((static_cast<uint32_t>(warp % 4) * 32) << 16) +
+                               static_cast<uint32_t>(256 * g + 128 * (gw / 4));
+        bool ok = true;
+        const int per_row = max(nchunks, 1);  // ring entries per row
+        const int total = sh.total;
+        for (int seq = g; seq < total; seq += kGroups) {  // this row's index in the cluster's sequence
+            int it = seq * per_row;
+            // ---------------- pass 1: chunks -> TMEM, slice max / first argmax, min
+            float best = -INFINITY, mn = INFINITY;
+            int be = 0x7fffffff;  // slice element of the first maximum
+            bool landed = true;
+            for (int c = 0; c < per_row; ++c, ++it) {
+                const int s = it % kSlots;
+                landed = __all_sync(0xffffffffu, landed && mbar_wait(&sh.full[s], (it / kSlots) & 1, limit));
+                if (!landed) break;
+                const float* sl = ring + static_cast<size_t>(s) * kChunk;
+                const int lo = c * kChunk;
+                const int n = cnt - lo;  // logits of this chunk (may exceed kChunk)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // two halves of 32 logits
+                    uint32_t rr[32];
+                    int bu = -1;
+                    float hb = best;
+#pragma unroll
+                    for (int u8 = 0; u8 < 8; ++u8) {
+                        const int u = h * 8 + u8;
+                        const int e = (u * kGroupThreads + gt) * 4;
+                        const float4 x = e < n ? *reinterpret_cast<const float4*>(sl + e)
+                                               : make_float4(-INFINITY, -INFINITY, -INFINITY,
+                                                             -INFINITY);
+                        const float gmx = fmaxf(max3(x.x, x.y, x.z), x.w);
+                        mn = fminf(mn, fminf(fminf(x.x, x.y), fminf(x.z, x.w)));
+                        if (gmx > hb) { hb = gmx; bu = u; }
+                        rr[4 * u8 + 0] = __float_as_uint(x.x);
+                        rr[4 * u8 + 1] = __float_as_uint(x.y);
+                        rr[4 * u8 + 2] = __float_as_uint(x.z);
+                        rr[4 * u8 + 3] = __float_as_uint(x.w);
+                    }
+                    if (bu >= 0) {  // a new maximum in this half: find its first component
+                        const int e = (bu * kGroupThreads + gt) * 4;
+                        const float4 x = *reinterpret_cast<const float4*>(sl + e);
+                        const int jj = x.x == hb ? 0 : x.y == hb ? 1 : x.z == hb ? 2 : 3;
+                        best = hb;
+                        be = lo + e + jj;
+                    }
+                    tmem_st32(tbase + 64 * c + 32 * h, rr);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.empty[s]);  // this warp is done with the slot
+            }
+            if (!named_bar_and(bar_id, kGroupThreads, landed)) { ok = false; break; }
+            const int q = seq % kXchg;
+            const uint32_t par = (seq / kXchg) & 1;
+
+            unsigned long long am = be < cnt ? enc_argmax(best, v0 + be) : 0ull;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) am = max(am, shfl_xor64(am, o));
+            if (lane == 0) sh.red_am[g][gw] = am;
+            named_bar_sync(bar_id, kGroupThreads);
+            if (gw == 0) {
+                unsigned long long a = sh.red_am[g][lane & 7];
+                a = max(a, shfl_xor64(a, 4));
+                a = max(a, shfl_xor64(a, 2));
+                a = max(a, shfl_xor64(a, 1));
+                bool free = true;
+                // CTA 0 reuses exchange slot q only once the collector is done with it.
+                if (rank == 0 && seq >= kXchg && lane == 0)
+                    free = mbar_wait(&sh.col_done[q], ((seq / kXchg) - 1) & 1, limit);
+                free = __shfl_sync(0xffffffffu, free, 0);
+                if (!free) ok = false;
+                if (free && lane < kCommitCluster) {  // lane j sends to CTA j
+                    st_cluster_u64(mapa_shared(smem_u32(&sh.am_in[q][rank]), lane), a);
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&sh.am_bar[q]), lane));
+                }
+            }
+            const bool got = ok && mbar_wait_cluster(&sh.am_bar[q], par, limit);
+            unsigned long long rm = sh.am_in[q][0];
+#pragma unroll
+            for (int k = 1; k < kCommitCluster; ++k) rm = max(rm, sh.am_in[q][k]);
+            const float m = dec_value(rm);
+
+            // ---------------- pass 2: fixed-point confidence terms, from TMEM
+            // Differences x = l - m below -31 have term 0; they are clamped
+            // there (keeps n and the exponent arithmetic in range) unless no
+            // logit of the warp needs it. Padding (-inf) clamps to a zero term,
+            // so every thread adds exactly 32 terms per column block read.
+            const f2 m2 = dup(m);
+            unsigned hi = 0, lo = 0, nterm = 0;
+            const bool noclamp = __all_sync(0xffffffffu, mn - m >= -31.0f);
+            const int ncol = 64 * nchunks;  // columns written for this row
+            for (int c0 = 0; c0 < ncol; c0 += 32) {
+                uint32_t rr[32];
+                tmem_ld32(tbase + c0, rr);
+                if (noclamp) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2)
+                        add_terms(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2),
+                                  hi, lo);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        float d0, d1;
+                        upk(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2), d0, d1);
+                        add_terms(pk(fmaxf(d0, -31.0f), fmaxf(d1, -31.0f)), hi, lo);
+                    }
+                }
+                nterm += 32;
+            }
+            hi -= nterm * kMagic43Bits;
+            lo -= nterm * kMagic23Bits;
+            unsigned long long acc = (static_cast<unsigned long long>(hi) << 20) +
+                                     static_cast<long long>(static_cast<int>(lo));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += shfl_xor64(acc, o);
+            if (lane == 0) sh.red_sum[g][gw] = acc;
+            if (!named_bar_and(bar_id, kGroupThreads, got)) { ok = false; break; }
+            if (gw == 0) {
+                unsigned long long a = sh.red_sum[g][lane & 7];
+                a += shfl_xor64(a, 4);
+                a += shfl_xor64(a, 2);
+                a += shfl_xor64(a, 1);
+                if (lane == 0) {
+                    if (rank == 0) sh.col_arg[q] = dec_index(rm);
+                    st_cluster_u64(mapa_shared(smem_u32(&sh.sum_in[q][rank]), 0), a);
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&sh.sum_bar[q]), 0));
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && gt == 0) atomicOr(p.status, kDevWaitTimeout);
+        __syncwarp();
+    }
+    // No CTA leaves while another may still write into its shared memory.
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(sh.tmem, 512);
+    }
 }
 
 }  // namespace
 
-size_t commit_smem_bytes(int V, int L) {
-    const size_t slice = static_cast<size_t>((((V + kCommitCluster - 1) / kCommitCluster) + 3) & ~3) * 4;
-    const size_t sel = static_cast<size_t>(L) * 9;
-    return slice > sel ? slice : sel;
+size_t commit_smem_bytes(int /*V*/, int /*L*/) {
+    return static_cast<size_t>(kSlots) * kChunk * 4 + static_cast<size_t>(kSelChunk) * 8 +
+           2 * (kCommitMaxL / 32) * 4;
+}
+
+int commit_max_clusters() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cached[dev] > 0) return cached[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCommitCluster * 256, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = commit_smem_bytes(kCommitCluster * kCommitSliceMax, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, commit_kernel, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        n = sms / kCommitCluster > 0 ? sms / kCommitCluster : 1;
+    }
+    cached[dev] = n;
+    return n;
 }
 
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t s) {
-    commit_kernel<<<static_cast<unsigned>(p.B * p.L) * kCommitCluster, kCommitThreads,
+    const long rows = static_cast<long>(p.B) * p.L;
+    const int ncl = static_cast<int>(rows < commit_max_clusters() ? rows : commit_max_clusters());
+    commit_kernel<<<static_cast<unsigned>(ncl) * kCommitCluster, kThreads,
                     commit_smem_bytes(p.V, p.L), s>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t configure_commit_kernels() {
     return cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kCommitSmemMax);
+                                static_cast<int>(commit_smem_bytes(kCommitCluster * kCommitSliceMax, 1)));
 }
 
 }  // namespace tt

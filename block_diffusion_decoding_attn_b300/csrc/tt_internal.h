@@ -54,15 +54,13 @@ struct CommitParams {
     unsigned long long timeout_ns;
 };
 
-constexpr int kCommitCluster = 8;       // CTAs sharing one logit row
-constexpr int kCommitThreads = 256;
-constexpr int kCommitSliceMax = 16384;  // fp32 logits per CTA (64 KB of shared memory)
-constexpr int kCommitMaxL = 16384;      // rows per block (the selection keeps 9 bytes/row in smem)
-constexpr int kCommitSmemMax = kCommitMaxL * 9 > kCommitSliceMax * 4 ? kCommitMaxL * 9
-                                                                      : kCommitSliceMax * 4;
+constexpr int kCommitCluster = 4;       // CTAs sharing one logit row
+constexpr int kCommitSliceMax = 32768;  // fp32 logits per CTA (a quarter row at V = 131072)
+constexpr int kCommitMaxL = 16384;      // rows per block
 
 size_t commit_smem_bytes(int V, int L);
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t s);
+int commit_max_clusters();  // co-resident clusters of the commit kernel (current device)
 cudaError_t configure_commit_kernels();
 cudaError_t configure_attn_kernels();
 

@@ -142,7 +142,9 @@ int tt_block_attn(tt_handle handle, const tt_attn_desc* desc, const void* q, con
  * align256(8*B*L) + align256(4*B*L). key/arg hold, after the call, the key and
  * prediction of every row that was masked on entry. The tickets must be ZERO
  * before a workspace is first used (e.g. cudaMemset); every call leaves them
- * zero again, so a workspace is zeroed once, not per call.
+ * zero again, so a workspace is zeroed once, not per call. After a call that
+ * set TT_DEV_WAIT_TIMEOUT the tickets are undefined: zero them again.
+ * Calls that share a workspace must not overlap on the GPU.
  * ------------------------------------------------------------------------ */
 size_t tt_commit_workspace_bytes(int B, int L);
 
