@@ -12,9 +12,10 @@
 // (key, row) and the first min(k, #masked) are committed: tok[r] = arg[r],
 // masked_out[r] = 0.
 //
-// Layout of the work: a persistent grid of 4-CTA clusters. Cluster c owns the
-// rows r = c, c + #clusters, ...; CTA j of the cluster owns the j-th quarter
-// of every row (128 KB at V = 131072). Per CTA:
+// Layout of the work: a persistent grid of 4-CTA clusters. Cluster c owns a
+// contiguous share of the masked rows (by ordinal; the shares differ by at
+// most one row); CTA j of the cluster owns the j-th quarter of each of its
+// rows (128 KB at V = 131072). Per CTA:
 //   warp 16 (producer): for each owned masked row, bulk TMA copies of the
 //       CTA's quarter in 64 KB chunks into a 3-slot shared-memory ring (L2
 //       evict-first); unmasked rows are only marked in masked_out;
@@ -75,18 +76,22 @@ constexpr unsigned kMagic43Bits = 0x55400000u;
 
 constexpr int kSlots = 3;                 // ring depth: 64 KB chunks landing per CTA
 constexpr int kChunk = 16384;             // logits per ring slot
-constexpr int kGroupThreads = 256;        // one consumer group: 8 warps
-constexpr int kGroups = 2;                // consumer groups, alternate rows
-constexpr int kConsumers = kGroups * kGroupThreads;
-constexpr int kProducerWarp = kConsumers / 32;      // warp 16
-constexpr int kCollectorWarp = kProducerWarp + 1;   // warp 17 (CTA 0 only)
-constexpr int kThreads = kConsumers + 64;
 constexpr int kSliceMax = 2 * kChunk;               // 32768 logits per CTA
-constexpr int kColsPerThread = kSliceMax / kGroupThreads * 2 / 2;  // 128 TMEM columns
+constexpr int kRowCols = kSliceMax / 128;           // 256 TMEM columns per row slot, 2 slots
+constexpr int kP1Warps = 8;               // pass 1: warps 0-7 (two per TMEM lane quarter)
+constexpr int kP2Warps = 8;               // pass 2: warps 8-15
+constexpr int kP1Threads = kP1Warps * 32;
+constexpr int kP2Threads = kP2Warps * 32;
+constexpr int kProducerWarp = kP1Warps + kP2Warps;  // warp 16
+constexpr int kCollectorWarp = kProducerWarp + 1;   // warp 17 (CTA 0 only)
+constexpr int kP1PerChunk = kChunk / kP1Threads;    // logits per pass-1 thread per chunk
+constexpr int kP2Cols = kRowCols / (kP2Warps / 4);  // TMEM columns per pass-2 thread
+constexpr int kThreads = (kCollectorWarp + 1) * 32;
 constexpr int kXchg = 8;                  // exchange slots (rows in flight in the cluster)
 constexpr int kSelChunk = 2048;           // keys staged per selection pass
+constexpr uint32_t kBarP1 = 1, kBarP2 = 2;  // named barriers of the two warp roles
 static_assert(kSliceMax == kCommitSliceMax, "slice per CTA");
-static_assert(kColsPerThread == 128, "two groups x two column halves x 128 = 512 TMEM columns");
+static_assert(2 * kRowCols == 512, "two row slots fill the TMEM");
 
 // Packed fp32 pairs: one f32x2 instruction does the same round-to-nearest
 // operation on both halves, halving the issue slots of the term arithmetic.
@@ -178,17 +183,22 @@ __device__ __forceinline__ unsigned long long shfl_xor64(unsigned long long v, i
 }
 
 struct CommitShared {
-    uint64_t full[kSlots];      // producer -> consumers: chunk landed
-    uint64_t empty[kSlots];     // consumers -> producer: slot free (8 warp arrivals)
+    uint64_t full[kSlots];      // producer -> pass 1: chunk landed
+    uint64_t empty[kSlots];     // pass 1 -> producer: slot free (one arrival per pass-1 warp)
+    uint64_t tfree[2];          // pass 2 -> pass 1: TMEM row slot free (one arrival per pass-2 warp)
     uint64_t am_bar[kXchg];     // one arrival per CTA: its slice (max, argmax)
     uint64_t sum_bar[kXchg];    // one arrival per CTA at CTA 0: its partial key
     uint64_t col_done[kXchg];   // CTA 0: the collector has finished the row
     unsigned long long am_in[kXchg][kCommitCluster];   // written by the cluster's CTAs
     unsigned long long sum_in[kXchg][kCommitCluster];  // (CTA 0 only)
     int col_arg[kXchg];                                 // (CTA 0) prediction of the row
-    unsigned long long red_am[kGroups][kGroupThreads / 32];
-    unsigned long long red_sum[kGroups][kGroupThreads / 32];
+    float smin[2];                                      // slice minimum of each TMEM row slot
+    unsigned long long red_am[kP1Warps];
+    float red_min[kP1Warps];
+    unsigned long long red_sum[kP2Warps];
     int total;              // masked rows of this cluster
+    int row0;               // first row of this cluster's range
+    int wsum[kThreads / 32];  // start-up scan: masked rows per warp
     uint32_t tmem;          // TMEM base address (512 columns)
 };
 
@@ -312,8 +322,10 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
     if (tid == 0) {
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], kGroupThreads / 32);
+            mbar_init(&sh.empty[s], kP1Warps);
         }
+        mbar_init(&sh.tfree[0], kP2Warps);
+        mbar_init(&sh.tfree[1], kP2Warps);
         for (int q = 0; q < kXchg; ++q) {
             mbar_init(&sh.am_bar[q], kCommitCluster);
             mbar_init(&sh.sum_bar[q], kCommitCluster);
@@ -325,12 +337,48 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
         tmem_alloc(&sh.tmem, 512);
         tmem_relinquish();
     }
-    if (warp == kProducerWarp) {  // the cluster's masked rows (every role loops to this count)
+    // The cluster's share of the rows: the masked rows with ordinals
+    // [cid * M / ncl, (cid + 1) * M / ncl) (M = masked rows in total), and the
+    // unmasked rows from the cluster's first masked row (row 0 for cluster 0)
+    // up to the next cluster's first one. Every role of every CTA of the
+    // cluster walks these rows in order; contiguous shares keep the blocks a
+    // cluster touches (and so its block tickets) few. Thread tid counts
+    // rows [tid * S, tid * S + S); a block-wide scan of the counts finds M and
+    // the thread that holds ordinal cid * M / ncl finds its row.
+    {
+        const int S = (rows + kThreads - 1) / kThreads;
+        const int r_lo = min(rows, tid * S), r_hi = min(rows, r_lo + S);
         int c = 0;
-        for (int r = cid + lane * ncl; r < rows; r += 32 * ncl) c += __ldcg(p.masked + r) != 0;
+        for (int r = r_lo; r < r_hi; ++r) c += __ldcg(p.masked + r) != 0;
+        int incl = c;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        if (lane == 0) sh.total = c;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) sh.wsum[warp] = incl;
+        __syncthreads();
+        int wpre = 0, mtot = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const int v = sh.wsum[w];
+            wpre += w < warp ? v : 0;
+            mtot += v;
+        }
+        const int excl = wpre + incl - c;
+        const int o0 = static_cast<int>(static_cast<long long>(cid) * mtot / ncl);
+        const int o1 = static_cast<int>(static_cast<long long>(cid + 1) * mtot / ncl);
+        if (tid == 0) {
+            sh.total = o1 - o0;
+            if (cid == 0 || o0 >= mtot) sh.row0 = cid == 0 ? 0 : rows;
+        }
+        if (cid > 0 && o0 < mtot && excl <= o0 && o0 < excl + c) {
+            int seen = excl;
+            for (int r = r_lo; r < r_hi; ++r)
+                if (__ldcg(p.masked + r) != 0 && seen++ == o0) {
+                    sh.row0 = r;
+                    break;
+                }
+        }
     }
     tc_fence_before();
     // Every CTA's barriers are initialised before any remote arrival.
@@ -347,13 +395,17 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
             const int per_row = max(nchunks, 1);
             int it = 0;  // ring entries issued
             bool ok = true;
-            for (int r = cid; r < rows && ok; r += ncl) {
+            const int total = sh.total;
+            int done = 0;
+            for (int r = sh.row0; r < rows && ok; ++r) {
                 // masked may alias masked_out: this read precedes the block's
                 // selection, which waits for this row's ticket.
                 if (__ldcg(p.masked + r) == 0) {
                     if (rank == 0) p.masked_out[r] = 0;
                     continue;
                 }
+                if (done == total) break;  // the next cluster's first row
+                ++done;
                 for (int c = 0; c < per_row; ++c, ++it) {
                     const int s = it % kSlots;
                     if (it >= kSlots && !mbar_wait(&sh.empty[s], ((it / kSlots) - 1) & 1, limit)) {
@@ -403,7 +455,8 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 if (__shfl_sync(0xffffffffu, last, 0))
                     select_block(p, cb, cnum, s_key, s_mbits, s_cbits, lane);
             };
-            for (int r = cid; r < rows; r += ncl) {
+            const int total = sh.total;
+            for (int r = sh.row0; r < rows && it < total; ++r) {
                 if (__ldcg(p.masked + r) == 0) continue;
                 const int q = it % kXchg;
                 if (!mbar_wait_cluster(&sh.sum_bar[q], (it / kXchg) & 1, limit)) {
@@ -435,150 +488,188 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------------------------- consumers
-        // Group g takes rows g, g + 2, ... of the cluster's sequence. Every
-        // named barrier of the group also ANDs the threads' wait results, so
-        // a wait that gave up in any thread ends the group's loop in all of
-        // them at the same barrier.
-        const int g = warp / (kGroupThreads / 32);
-        const int gw = warp % (kGroupThreads / 32);
-        const int gt = tid % kGroupThreads;
-        const uint32_t bar_id = 1 + g;
-        // This thread's TMEM: lane 32 * (warp % 4) + lane, 128 columns from
-        // 256 g + 128 (gw / 4). Chunk c of the slice lands in columns
-        // 64 c .. 64 c + 63 of them: float4 u of the chunk (slice element
-        // c * kChunk + 4 * (u * 256 + gt)) in columns 64 c + 4 u .. + 3, so
-        // the columns run in slice order for every thread.
-        const uint32_t tbase = sh.tmem + ((static_cast<uint32_t>(warp % 4) * 32) << 16) +
-                               static_cast<uint32_t>(256 * g + 128 * (gw / 4));
-        bool ok = true;
+        // ---------------------------------------------------------------- pass 1 / pass 2
+        // Rows of the cluster's sequence alternate between the two TMEM row
+        // slots (256 columns each). Pass 1 (warps 0-3) drains a row's chunks
+        // from the ring into its slot, taking the slice max / first argmax /
+        // min, and sends the result to the cluster; pass 2 (warps 4-11) waits
+        // for the cluster's results of that row, sums its fixed-point terms
+        // from TMEM and frees the slot. So pass 1 of row i + 1 and the
+        // exchange run while pass 2 works on row i. Every named barrier also
+        // ANDs the threads' wait results: a wait that gave up in any thread
+        // ends the loop of all the threads of that role at the same barrier.
         const int per_row = max(nchunks, 1);  // ring entries per row
         const int total = sh.total;
-        for (int seq = g; seq < total; seq += kGroups) {  // this row's index in the cluster's sequence
-            int it = seq * per_row;
-            // ---------------- pass 1: chunks -> TMEM, slice max / first argmax, min
-            float best = -INFINITY, mn = INFINITY;
-            int be = 0x7fffffff;  // slice element of the first maximum
-            bool landed = true;
-            for (int c = 0; c < per_row; ++c, ++it) {
-                const int s = it % kSlots;
-                landed = __all_sync(0xffffffffu, landed && mbar_wait(&sh.full[s], (it / kSlots) & 1, limit));
-                if (!landed) break;
-                const float* sl = ring + static_cast<size_t>(s) * kChunk;
-                const int lo = c * kChunk;
-                const int n = cnt - lo;  // logits of this chunk (may exceed kChunk)
+        bool ok = true;
+        if (warp < kP1Warps) {
+            // ------------------------------------------------------------ pass 1
+            // Thread pt writes TMEM lane pt % 128. Chunk c of the row goes to
+            // columns 128 c .. 128 c + 127 of the slot, kP1PerChunk of them
+            // from 128 c + kP1PerChunk * (pt / 128) for this thread: float4 u of
+            // the chunk (slice element c * kChunk + 4 * (u * kP1Threads + pt))
+            // in 4 columns from there + 4 u, so the columns run in slice order
+            // for every thread. (Pass 2 only sums, so it reads them in any order.)
+            const int pt = tid;
+            const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
+            const int csub = kP1PerChunk * (pt / 128);
+            for (int seq = 0; seq < total; ++seq) {
+                const int t = seq & 1;
+                bool good = ok;
+                if (seq >= 2) good = good && mbar_wait(&sh.tfree[t], ((seq >> 1) - 1) & 1, limit);
+                good = __all_sync(0xffffffffu, good);
+                tc_fence_after();
+                const uint32_t tb = sh.tmem + lane_off + static_cast<uint32_t>(t * kRowCols + csub);
+                float best = -INFINITY, mn = INFINITY;
+                int be = 0x7fffffff;  // slice element of the first maximum
+                int it = seq * per_row;
+                for (int c = 0; c < per_row && good; ++c, ++it) {
+                    const int s = it % kSlots;
+                    good = __all_sync(0xffffffffu, mbar_wait(&sh.full[s], (it / kSlots) & 1, limit));
+                    if (!good) break;
+                    const float* sl = ring + static_cast<size_t>(s) * kChunk;
+                    const int lo = c * kChunk;
+                    const int n = cnt - lo;  // logits of this chunk (may exceed kChunk)
+#pragma unroll 1
+                    for (int h = 0; h < kP1PerChunk / 32; ++h) {  // groups of 32 logits
+                        uint32_t rr[32];
+                        int bu = -1;
+                        float hb = best;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {  // two halves of 32 logits
-                    uint32_t rr[32];
-                    int bu = -1;
-                    float hb = best;
-#pragma unroll
-                    for (int u8 = 0; u8 < 8; ++u8) {
-                        const int u = h * 8 + u8;
-                        const int e = (u * kGroupThreads + gt) * 4;
-                        const float4 x = e < n ? *reinterpret_cast<const float4*>(sl + e)
-                                               : make_float4(-INFINITY, -INFINITY, -INFINITY,
-                                                             -INFINITY);
-                        const float gmx = fmaxf(max3(x.x, x.y, x.z), x.w);
-                        mn = fminf(mn, fminf(fminf(x.x, x.y), fminf(x.z, x.w)));
-                        if (gmx > hb) { hb = gmx; bu = u; }
-                        rr[4 * u8 + 0] = __float_as_uint(x.x);
-                        rr[4 * u8 + 1] = __float_as_uint(x.y);
-                        rr[4 * u8 + 2] = __float_as_uint(x.z);
-                        rr[4 * u8 + 3] = __float_as_uint(x.w);
+                        for (int u8 = 0; u8 < 8; ++u8) {
+                            const int u = h * 8 + u8;
+                            const int e = (u * kP1Threads + pt) * 4;
+                            const float4 x = e < n ? *reinterpret_cast<const float4*>(sl + e)
+                                                   : make_float4(-INFINITY, -INFINITY, -INFINITY,
+                                                                 -INFINITY);
+                            const float gmx = fmaxf(max3(x.x, x.y, x.z), x.w);
+                            mn = fminf(mn, fminf(fminf(x.x, x.y), fminf(x.z, x.w)));
+                            if (gmx > hb) { hb = gmx; bu = u; }
+                            rr[4 * u8 + 0] = __float_as_uint(x.x);
+                            rr[4 * u8 + 1] = __float_as_uint(x.y);
+                            rr[4 * u8 + 2] = __float_as_uint(x.z);
+                            rr[4 * u8 + 3] = __float_as_uint(x.w);
+                        }
+                        if (bu >= 0) {  // a new maximum in this group: its first component
+                            const int e = (bu * kP1Threads + pt) * 4;
+                            const float4 x = *reinterpret_cast<const float4*>(sl + e);
+                            const int jj = x.x == hb ? 0 : x.y == hb ? 1 : x.z == hb ? 2 : 3;
+                            best = hb;
+                            be = lo + e + jj;
+                        }
+                        tmem_st32(tb + 128 * c + 32 * h, rr);
                     }
-                    if (bu >= 0) {  // a new maximum in this half: find its first component
-                        const int e = (bu * kGroupThreads + gt) * 4;
-                        const float4 x = *reinterpret_cast<const float4*>(sl + e);
-                        const int jj = x.x == hb ? 0 : x.y == hb ? 1 : x.z == hb ? 2 : 3;
-                        best = hb;
-                        be = lo + e + jj;
-                    }
-                    tmem_st32(tbase + 64 * c + 32 * h, rr);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.empty[s]);  // this warp is done with the slot
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.empty[s]);  // this warp is done with the slot
-            }
-            if (!named_bar_and(bar_id, kGroupThreads, landed)) { ok = false; break; }
-            const int q = seq % kXchg;
-            const uint32_t par = (seq / kXchg) & 1;
-
-            unsigned long long am = be < cnt ? enc_argmax(best, v0 + be) : 0ull;
+                unsigned long long am = be < cnt ? enc_argmax(best, v0 + be) : 0ull;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) am = max(am, shfl_xor64(am, o));
-            if (lane == 0) sh.red_am[g][gw] = am;
-            named_bar_sync(bar_id, kGroupThreads);
-            if (gw == 0) {
-                unsigned long long a = sh.red_am[g][lane & 7];
-                a = max(a, shfl_xor64(a, 4));
-                a = max(a, shfl_xor64(a, 2));
-                a = max(a, shfl_xor64(a, 1));
-                bool free = true;
-                // CTA 0 reuses exchange slot q only once the collector is done with it.
-                if (rank == 0 && seq >= kXchg && lane == 0)
-                    free = mbar_wait(&sh.col_done[q], ((seq / kXchg) - 1) & 1, limit);
-                free = __shfl_sync(0xffffffffu, free, 0);
-                if (!free) ok = false;
-                if (free && lane < kCommitCluster) {  // lane j sends to CTA j
-                    st_cluster_u64(mapa_shared(smem_u32(&sh.am_in[q][rank]), lane), a);
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&sh.am_bar[q]), lane));
+                for (int o = 16; o > 0; o >>= 1) {
+                    am = max(am, shfl_xor64(am, o));
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
                 }
-            }
-            const bool got = ok && mbar_wait_cluster(&sh.am_bar[q], par, limit);
-            unsigned long long rm = sh.am_in[q][0];
-#pragma unroll
-            for (int k = 1; k < kCommitCluster; ++k) rm = max(rm, sh.am_in[q][k]);
-            const float m = dec_value(rm);
-
-            // ---------------- pass 2: fixed-point confidence terms, from TMEM
-            // Differences x = l - m below -31 have term 0; they are clamped
-            // there (keeps n and the exponent arithmetic in range) unless no
-            // logit of the warp needs it. Padding (-inf) clamps to a zero term,
-            // so every thread adds exactly 32 terms per column block read.
-            const f2 m2 = dup(m);
-            unsigned hi = 0, lo = 0, nterm = 0;
-            const bool noclamp = __all_sync(0xffffffffu, mn - m >= -31.0f);
-            const int ncol = 64 * nchunks;  // columns written for this row
-            for (int c0 = 0; c0 < ncol; c0 += 32) {
-                uint32_t rr[32];
-                tmem_ld32(tbase + c0, rr);
-                if (noclamp) {
-#pragma unroll
-                    for (int k = 0; k < 32; k += 2)
-                        add_terms(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2),
-                                  hi, lo);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; k += 2) {
-                        float d0, d1;
-                        upk(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2), d0, d1);
-                        add_terms(pk(fmaxf(d0, -31.0f), fmaxf(d1, -31.0f)), hi, lo);
-                    }
-                }
-                nterm += 32;
-            }
-            hi -= nterm * kMagic43Bits;
-            lo -= nterm * kMagic23Bits;
-            unsigned long long acc = (static_cast<unsigned long long>(hi) << 20) +
-                                     static_cast<long long>(static_cast<int>(lo));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc += shfl_xor64(acc, o);
-            if (lane == 0) sh.red_sum[g][gw] = acc;
-            if (!named_bar_and(bar_id, kGroupThreads, got)) { ok = false; break; }
-            if (gw == 0) {
-                unsigned long long a = sh.red_sum[g][lane & 7];
-                a += shfl_xor64(a, 4);
-                a += shfl_xor64(a, 2);
-                a += shfl_xor64(a, 1);
                 if (lane == 0) {
-                    if (rank == 0) sh.col_arg[q] = dec_index(rm);
-                    st_cluster_u64(mapa_shared(smem_u32(&sh.sum_in[q][rank]), 0), a);
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&sh.sum_bar[q]), 0));
+                    sh.red_am[warp] = am;
+                    sh.red_min[warp] = mn;
                 }
+                tc_fence_before();
+                if (!named_bar_and(kBarP1, kP1Threads, good)) { ok = false; break; }
+                if (warp == 0) {
+                    const int q = seq % kXchg;
+                    unsigned long long a = lane < kP1Warps ? sh.red_am[lane] : 0ull;
+                    float mnv = lane < kP1Warps ? sh.red_min[lane] : INFINITY;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        a = max(a, shfl_xor64(a, o));
+                        mnv = fminf(mnv, __shfl_xor_sync(0xffffffffu, mnv, o));
+                    }
+                    bool free = true;
+                    // CTA 0 reuses exchange slot q only once the collector is done with it.
+                    if (rank == 0 && seq >= kXchg && lane == 0)
+                        free = mbar_wait(&sh.col_done[q], ((seq / kXchg) - 1) & 1, limit);
+                    free = __shfl_sync(0xffffffffu, free, 0);
+                    if (!free) ok = false;
+                    if (free && lane < kCommitCluster) {  // lane j sends to CTA j
+                        if (lane == static_cast<int>(rank)) sh.smin[t] = mnv;  // released with it
+                        st_cluster_u64(mapa_shared(smem_u32(&sh.am_in[q][rank]), lane), a);
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&sh.am_bar[q]), lane));
+                    }
+                    __syncwarp();
+                }
+            }
+        } else {
+            // ------------------------------------------------------------ pass 2
+            // Warp pw reads TMEM lanes 32 (pw % 4) .. + 31 and kP2Cols columns
+            // of the slot from kP2Cols * (pw / 4) (inside chunk
+            // kP2Cols * (pw / 4) / 128 of the row).
+            const int pw = warp - kP1Warps;
+            const int c0w = kP2Cols * (pw / 4);
+            const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
+            const int ncol = c0w / 128 < nchunks ? kP2Cols : 0;
+            for (int seq = 0; seq < total; ++seq) {
+                const int t = seq & 1;
+                const int q = seq % kXchg;
+                const bool got = __all_sync(
+                    0xffffffffu, ok && mbar_wait_cluster(&sh.am_bar[q], (seq / kXchg) & 1, limit));
+                tc_fence_after();
+                unsigned long long rm = sh.am_in[q][0];
+#pragma unroll
+                for (int k = 1; k < kCommitCluster; ++k) rm = max(rm, sh.am_in[q][k]);
+                const float m = dec_value(rm);
+                // Differences x = l - m below -31 have term 0; they are clamped
+                // there (keeps n and the exponent arithmetic in range) unless no
+                // logit of the slice needs it. Padding (-inf) clamps to a zero
+                // term, so every thread adds exactly ncol terms.
+                const bool noclamp = sh.smin[t] - m >= -31.0f;
+                const f2 m2 = dup(m);
+                unsigned hi = 0, lo = 0;
+                const uint32_t tb = sh.tmem + lane_off + static_cast<uint32_t>(t * kRowCols + c0w);
+                if (got) {
+                    for (int c0 = 0; c0 < ncol; c0 += 32) {
+                        uint32_t rr[32];
+                        tmem_ld32(tb + c0, rr);
+                        if (noclamp) {
+#pragma unroll
+                            for (int k = 0; k < 32; k += 2)
+                                add_terms(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2),
+                                          hi, lo);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 32; k += 2) {
+                                float d0, d1;
+                                upk(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2),
+                                    d0, d1);
+                                add_terms(pk(fmaxf(d0, -31.0f), fmaxf(d1, -31.0f)), hi, lo);
+                            }
+                        }
+                    }
+                }
+                hi -= static_cast<unsigned>(ncol) * kMagic43Bits;
+                lo -= static_cast<unsigned>(ncol) * kMagic23Bits;
+                unsigned long long acc = (static_cast<unsigned long long>(hi) << 20) +
+                                         static_cast<long long>(static_cast<int>(lo));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc += shfl_xor64(acc, o);
+                tc_fence_before();
                 __syncwarp();
+                if (lane == 0) {
+                    sh.red_sum[pw] = acc;
+                    if (got) mbar_arrive(&sh.tfree[t]);  // this warp is done with the slot
+                }
+                if (!named_bar_and(kBarP2, kP2Threads, got)) { ok = false; break; }
+                if (pw == 0) {
+                    unsigned long long a = lane < kP2Warps ? sh.red_sum[lane] : 0ull;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) a += shfl_xor64(a, o);
+                    if (lane == 0) {
+                        if (rank == 0) sh.col_arg[q] = dec_index(rm);
+                        st_cluster_u64(mapa_shared(smem_u32(&sh.sum_in[q][rank]), 0), a);
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&sh.sum_bar[q]), 0));
+                    }
+                    __syncwarp();
+                }
             }
         }
-        if (!ok && gt == 0) atomicOr(p.status, kDevWaitTimeout);
+        if (!ok && (tid == 0 || tid == kP1Threads)) atomicOr(p.status, kDevWaitTimeout);
         __syncwarp();
     }
     // No CTA leaves while another may still write into its shared memory.
