@@ -213,6 +213,69 @@ struct CommitShared {
 //   L <= kSelChunk: k rounds of a warp argmin over the keys staged in shared
 //       memory, each round taking the smallest (key, row) above the last;
 //   larger L: each row's rank is counted over the keys, chunk by chunk.
+// L <= 256: every lane holds up to 8 rows (row 32 q + lane) in registers;
+// flags, keys and predictions come in one round trip of loads.
+constexpr int kSelRegRows = 8;
+
+__device__ void select_block_small(const CommitParams& p, int b, int n, int lane) {
+    const size_t base = static_cast<size_t>(b) * p.L;
+    bool mi[kSelRegRows];
+    unsigned long long ki[kSelRegRows];
+    int ai[kSelRegRows];
+#pragma unroll
+    for (int q = 0; q < kSelRegRows; ++q) {
+        const int i = q * 32 + lane;
+        mi[q] = false;
+        ki[q] = ~0ull;
+        ai[q] = 0;
+        if (i < p.L) {
+            mi[q] = __ldcg(p.masked + base + i) != 0;
+            ki[q] = __ldcg(p.key + base + i);
+            ai[q] = __ldcg(p.arg + base + i);
+        }
+    }
+    uint32_t commit = 0;  // bit q: row 32 q + lane is committed
+#pragma unroll
+    for (int q = 0; q < kSelRegRows; ++q) {
+        if (!mi[q]) ki[q] = ~0ull;  // unmasked rows never rank
+        if (n <= p.k && mi[q]) commit |= 1u << q;
+    }
+    if (n > p.k) {
+        unsigned long long lk = 0;  // last chosen (key, row); row -1: none yet
+        int lr = -1;
+        for (int round = 0; round < p.k; ++round) {
+            unsigned long long bk = ~0ull;
+            int br = 0x7fffffff;
+#pragma unroll
+            for (int q = 0; q < kSelRegRows; ++q) {
+                const int j = q * 32 + lane;
+                const bool above = ki[q] > lk || (ki[q] == lk && j > lr);
+                const bool below = ki[q] < bk || (ki[q] == bk && j < br);
+                if (ki[q] != ~0ull && above && below) { bk = ki[q]; br = j; }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long ok_ = __shfl_xor_sync(0xffffffffu, bk, o);
+                const int orow = __shfl_xor_sync(0xffffffffu, br, o);
+                if (ok_ < bk || (ok_ == bk && orow < br)) { bk = ok_; br = orow; }
+            }
+            if (br == 0x7fffffff) break;
+            if ((br & 31) == lane) commit |= 1u << (br >> 5);
+            lk = bk;
+            lr = br;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kSelRegRows; ++q) {
+        const int i = q * 32 + lane;
+        if (mi[q]) {
+            const bool c = (commit >> q) & 1u;
+            if (c) p.tok[base + i] = ai[q];
+            p.masked_out[base + i] = c ? 0 : 1;
+        }
+    }
+}
+
 __device__ void select_block(const CommitParams& p, int b, int n, unsigned long long* s_key,
                              uint32_t* s_mbits, uint32_t* s_cbits, int lane) {
     const size_t base = static_cast<size_t>(b) * p.L;
@@ -287,6 +350,12 @@ __device__ void select_block(const CommitParams& p, int b, int n, unsigned long 
         }
     }
     __syncwarp();
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* a, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+    return old;
 }
 
 // Masked rows of block b (read by one warp).
@@ -444,16 +513,17 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
             auto flush = [&]() {
                 int last = 0;
                 if (lane == 0) {
-                    __threadfence();  // the rows' key / arg before the ticket
-                    const unsigned t = atomicAdd(p.counters + cb, static_cast<unsigned>(cmine));
+                    // acq_rel: the rows' key / arg are visible before the ticket;
+                    // the last ticket sees every other cluster's rows.
+                    const unsigned t = atom_add_acq_rel_gpu(p.counters + cb, static_cast<unsigned>(cmine));
                     last = t + static_cast<unsigned>(cmine) == static_cast<unsigned>(cnum);
-                    if (last) {
-                        p.counters[cb] = 0;  // no other ticket of this call remains
-                        __threadfence();
-                    }
+                    if (last) p.counters[cb] = 0;  // no other ticket of this call remains
                 }
-                if (__shfl_sync(0xffffffffu, last, 0))
-                    select_block(p, cb, cnum, s_key, s_mbits, s_cbits, lane);
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __threadfence();  // every lane reads the other clusters' rows after the ticket
+                    if (p.L <= 32 * kSelRegRows) select_block_small(p, cb, cnum, lane);
+                    else select_block(p, cb, cnum, s_key, s_mbits, s_cbits, lane);
+                }
             };
             const int total = sh.total;
             for (int r = sh.row0; r < rows && it < total; ++r) {
