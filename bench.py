@@ -291,7 +291,7 @@ def run_gpu(args, w):
         flush_sum.copy_(flush.view(torch.int64).sum())
 
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 1 + (1 if ws_a_n > 0 else 0) + 2
+    launches_per_step = 1 + (1 if ws_a_n > 0 else 0) + 1  # attention (+ split merge) + commit
 
     def step():
         tt.block_attn(A["q"], A["k_blk"], A["v_blk"], A["k_ctx"], A["v_ctx"], A["ctx_len"],

@@ -401,44 +401,72 @@ __global__ void __launch_bounds__(320, 1)
 
 // Combines the per-split partials (running max m_s, running sum l_s,
 // unnormalised O_s) of sequences that were split: one warp per output row.
+// Launched as a programmatic dependent of the attention grid: the row's place
+// and its number of splits come from ctx_len alone, before waiting for that
+// grid; after the wait the splits are read in one pass, four at a time, with
+// an online rescale to the running maximum.
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     constexpr int kPer = D / 32;  // columns per lane
-    // Launched as a programmatic dependent of the attention grid: wait until
-    // that grid has completed and its partials are visible.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long gw = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const long rows_bk = static_cast<long>(p.G) * p.L;
-    if (gw >= rows_bk * p.B * p.Hkv) return;
-    const int m = static_cast<int>(gw % rows_bk);
-    const int bk = static_cast<int>(gw / rows_bk);
+    const bool valid = gw < rows_bk * p.B * p.Hkv;
+    const int m = valid ? static_cast<int>(gw % rows_bk) : 0;
+    const int bk = valid ? static_cast<int>(gw / rows_bk) : 0;
     const int kvh = bk % p.Hkv, b = bk / p.Hkv;
-    int C = p.ctx_len[b];
-    C = C < 0 ? 0 : (C > p.ctx_cap ? p.ctx_cap : C);
-    const int nt = (C + kTile - 1) / kTile + p.nblk;
-    const int ns = (nt + p.chunk - 1) / p.chunk;
-    if (ns == 1) return;  // written directly by the attention kernel
+    int ns = 0;
+    if (valid) {
+        int C = p.ctx_len[b];
+        C = C < 0 ? 0 : (C > p.ctx_cap ? p.ctx_cap : C);
+        const int nt = (C + kTile - 1) / kTile + p.nblk;
+        ns = (nt + p.chunk - 1) / p.chunk;
+    }
+    // Wait until the attention grid has completed and its partials are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (ns <= 1) return;  // not split: written directly by the attention kernel
     const size_t mpad = static_cast<size_t>(p.n_mtiles) * kTile;
     const size_t split_stride = static_cast<size_t>(p.B) * p.Hkv * mpad;
     const size_t base = (static_cast<size_t>(b) * p.Hkv + kvh) * mpad + m;
-    float mx = -INFINITY;
-    for (int s = 0; s < ns; ++s) mx = fmaxf(mx, p.ws_ml[(s * split_stride + base) * 2]);
-    float den = 0.f, acc[kPer];
+    float mx = -INFINITY, den = 0.f, acc[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
-    for (int s = 0; s < ns; ++s) {
-        const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (s * split_stride + base) * 2);
-        const float w = ex2_approx(ml.x - mx);
-        den += w * ml.y;
-        const float* o = p.ws_o + (s * split_stride + base) * D + lane * kPer;
-        if constexpr (kPer == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(o);
-            acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2*>(o);
-            acc[0] += w * v.x; acc[1] += w * v.y;
+    for (int s0 = 0; s0 < ns; s0 += 4) {
+        float pm[4], pl[4], pv[4][kPer];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            pm[u] = -INFINITY;
+            pl[u] = 0.f;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) pv[u][j] = 0.f;
+            if (s0 + u < ns) {
+                const size_t r = (s0 + u) * split_stride + base;
+                const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + r * 2));
+                pm[u] = ml.x;
+                pl[u] = ml.y;
+                const float* o = p.ws_o + r * D + lane * kPer;
+                if constexpr (kPer == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
+                    pv[u][0] = v.x; pv[u][1] = v.y; pv[u][2] = v.z; pv[u][3] = v.w;
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
+                    pv[u][0] = v.x; pv[u][1] = v.y;
+                }
+            }
         }
+        const float nm = fmaxf(fmaxf(mx, fmaxf(pm[0], pm[1])), fmaxf(pm[2], pm[3]));
+        const float sc = ex2_approx(mx - nm);  // 0 on the first round (mx = -inf)
+        den *= sc;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) acc[j] *= sc;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float w = ex2_approx(pm[u] - nm);  // 0 for the padding splits
+            den += w * pl[u];
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) acc[j] += w * pv[u][j];
+        }
+        mx = nm;
     }
     const float inv = 1.f / den;
     const int l = m / p.G, g = m % p.G;
