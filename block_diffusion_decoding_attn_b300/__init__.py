@@ -13,6 +13,8 @@ Entry points mirror the C ABI:
   Section 2.1, Eq. 1)
 * :func:`commit` -> ``tt_commit`` (Section 2.2, Algorithm 2 with k commits per
   block per step)
+* :func:`commit_threshold` -> ``tt_commit_threshold`` (Algorithm 2 with a
+  confidence threshold gamma and a floor of ceil(#masked / steps_left))
 """
 from __future__ import annotations
 
@@ -64,8 +66,9 @@ def lib() -> ctypes.CDLL:
             L.tt_commit_workspace_bytes.restype = S
             L.tt_commit_workspace_bytes.argtypes = [I, I]
             L.tt_commit.argtypes = [P, P, I, I, I, P, I, P, P, P, S, P]
+            L.tt_commit_threshold.argtypes = [P, P, I, I, I, P, ctypes.c_double, I, P, P, P, S, P]
             for f in ("tt_create", "tt_destroy", "tt_get_error", "tt_set_wait_timeout",
-                      "tt_block_attn", "tt_commit"):
+                      "tt_block_attn", "tt_commit", "tt_commit_threshold"):
                 getattr(L, f).restype = I
             _lib = L
     return _lib
@@ -216,6 +219,32 @@ def commit(logits, B: int, L: int, masked, k: int, tok, masked_out=None, workspa
                            _dev_ptr(masked), int(k), _dev_ptr(tok), _dev_ptr(masked_out),
                            _dev_ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream_ptr(logits, stream)), "tt_commit")
+    return tok, masked_out, workspace
+
+
+def commit_threshold(logits, B: int, L: int, masked, gamma: float, steps_left: int, tok,
+                     masked_out=None, workspace=None, h: Handle | None = None, stream=None):
+    """One threshold unmasking step (Algorithm 2): per block, every masked row
+    whose confidence is above gamma, and at least ceil(#masked / steps_left).
+
+    Arguments and results as :func:`commit`.
+    """
+    import torch
+    if logits.dtype != torch.float32 or not logits.is_cuda or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous CUDA float32 tensor")
+    if masked.dtype != torch.uint8 or tok.dtype != torch.int32:
+        raise ValueError("masked must be uint8 and tok int32")
+    h = h or handle(logits.device.index)
+    if masked_out is None:
+        masked_out = torch.empty_like(masked)
+    need = commit_workspace_bytes(B, L)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=logits.device)
+    _check(lib().tt_commit_threshold(h.ptr, _dev_ptr(logits), int(B), int(L), int(logits.shape[1]),
+                                     _dev_ptr(masked), float(gamma), int(steps_left), _dev_ptr(tok),
+                                     _dev_ptr(masked_out), _dev_ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream_ptr(logits, stream)), "tt_commit_threshold")
     return tok, masked_out, workspace
 
 

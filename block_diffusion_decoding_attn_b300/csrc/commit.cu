@@ -213,6 +213,14 @@ struct CommitShared {
 //   L <= kSelChunk: k rounds of a warp argmin over the keys staged in shared
 //       memory, each round taking the smallest (key, row) above the last;
 //   larger L: each row's rank is counted over the keys, chunk by chunk.
+// Rows block b commits, given its n masked rows and, in threshold mode, the
+// number of them whose key is <= kthr (cthr, the rows whose confidence is
+// above gamma: they are the first cthr rows of the (key, row) order).
+__device__ __forceinline__ int block_budget(const CommitParams& p, int n, int cthr) {
+    if (p.steps_left <= 0) return p.k;
+    return max(cthr, (n + p.steps_left - 1) / p.steps_left);
+}
+
 // L <= 256: every lane holds up to 8 rows (row 32 q + lane) in registers;
 // flags, keys and predictions come in one round trip of loads.
 constexpr int kSelRegRows = 8;
@@ -234,16 +242,23 @@ __device__ void select_block_small(const CommitParams& p, int b, int n, int lane
             ai[q] = __ldcg(p.arg + base + i);
         }
     }
-    uint32_t commit = 0;  // bit q: row 32 q + lane is committed
+    int cthr = 0;
 #pragma unroll
     for (int q = 0; q < kSelRegRows; ++q) {
         if (!mi[q]) ki[q] = ~0ull;  // unmasked rows never rank
-        if (n <= p.k && mi[q]) commit |= 1u << q;
+        cthr += (mi[q] && ki[q] <= p.kthr) ? 1 : 0;
     }
-    if (n > p.k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cthr += __shfl_xor_sync(0xffffffffu, cthr, o);
+    const int kb = block_budget(p, n, cthr);
+    uint32_t commit = 0;  // bit q: row 32 q + lane is committed
+#pragma unroll
+    for (int q = 0; q < kSelRegRows; ++q)
+        if (n <= kb && mi[q]) commit |= 1u << q;
+    if (n > kb) {
         unsigned long long lk = 0;  // last chosen (key, row); row -1: none yet
         int lr = -1;
-        for (int round = 0; round < p.k; ++round) {
+        for (int round = 0; round < kb; ++round) {
             unsigned long long bk = ~0ull;
             int br = 0x7fffffff;
 #pragma unroll
@@ -280,23 +295,27 @@ __device__ void select_block(const CommitParams& p, int b, int n, unsigned long 
                              uint32_t* s_mbits, uint32_t* s_cbits, int lane) {
     const size_t base = static_cast<size_t>(b) * p.L;
     const int nw = (p.L + 31) / 32;
+    int cthr = 0;
     for (int w = 0; w < nw; ++w) {
         const int i = w * 32 + lane;
         const bool mi = i < p.L && __ldcg(p.masked + base + i) != 0;
+        cthr += (mi && p.steps_left > 0 && __ldcg(p.key + base + i) <= p.kthr) ? 1 : 0;
         const uint32_t mb = __ballot_sync(0xffffffffu, mi);
-        if (lane == 0) {
-            s_mbits[w] = mb;
-            s_cbits[w] = n <= p.k ? mb : 0u;
-        }
+        if (lane == 0) s_mbits[w] = mb;
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cthr += __shfl_xor_sync(0xffffffffu, cthr, o);
+    const int kb = block_budget(p, n, cthr);
+    if (lane == 0)
+        for (int w = 0; w < nw; ++w) s_cbits[w] = n <= kb ? s_mbits[w] : 0u;
     __syncwarp();
-    if (n > p.k && p.L <= kSelChunk) {
+    if (n > kb && p.L <= kSelChunk) {
         for (int j = lane; j < p.L; j += 32)
             s_key[j] = (s_mbits[j >> 5] >> (j & 31)) & 1u ? __ldcg(p.key + base + j) : ~0ull;
         __syncwarp();
         unsigned long long lk = 0;  // last chosen (key, row); row -1: none yet
         int lr = -1;
-        for (int round = 0; round < p.k; ++round) {
+        for (int round = 0; round < kb; ++round) {
             unsigned long long bk = ~0ull;
             int br = 0x7fffffff;
             for (int j = lane; j < p.L; j += 32) {
@@ -316,7 +335,7 @@ __device__ void select_block(const CommitParams& p, int b, int n, unsigned long 
             lk = bk;
             lr = br;
         }
-    } else if (n > p.k) {
+    } else if (n > kb) {
         for (int w = 0; w < nw; ++w) {
             const int i = w * 32 + lane;
             const bool mi = (s_mbits[w] >> lane) & 1u;
@@ -336,7 +355,7 @@ __device__ void select_block(const CommitParams& p, int b, int n, unsigned long 
                     rank += (kj < ki || (kj == ki && j < lim)) ? 1 : 0;
                 }
             }
-            const uint32_t cb = __ballot_sync(0xffffffffu, mi && rank < p.k);
+            const uint32_t cb = __ballot_sync(0xffffffffu, mi && rank < kb);
             if (lane == 0) s_cbits[w] = cb;
         }
     }

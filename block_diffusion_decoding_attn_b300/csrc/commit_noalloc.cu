@@ -87,6 +87,8 @@ extern "C" int tt_commit_noalloc(const float* logits, int B, int L, int V, const
     p.L = L;
     p.V = V;
     p.k = k;
+    p.steps_left = 0;  // fixed budget of k
+    p.kthr = 0;
     p.slice = (((V + tt::kCommitCluster - 1) / tt::kCommitCluster) + 3) & ~3;  // per-CTA share
     p.masked = masked;
     p.tok = tok;

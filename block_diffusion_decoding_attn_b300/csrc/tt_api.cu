@@ -320,32 +320,57 @@ size_t tt_commit_workspace_bytes(int B, int L) {
     return align256(rows * 8) + align256(rows * 4) + static_cast<size_t>(B) * 4;
 }
 
-int tt_commit(tt_handle h, const float* logits, int B, int L, int V, const uint8_t* masked, int k,
-              int32_t* tok, uint8_t* masked_out, void* workspace, size_t workspace_bytes,
-              void* stream) {
-    if (!h) return fail(TT_ERR_INVALID_ARG, "tt_commit: handle is NULL");
-    if (B < 0) return fail(TT_ERR_INVALID_ARG, "tt_commit: B=%d < 0", B);
+}  // extern "C"
+
+namespace {
+
+// The largest key whose confidence 2^40 / key exceeds gamma, i.e. the largest
+// integer key with gamma * key < 2^40, in exact arithmetic: gamma = M *
+// 2^(e - 53) with an integer M (53 bits), so the condition is M * key <
+// 2^(93 - e), decided on 128-bit integers. gamma <= 0: every key; gamma = +inf
+// or a gamma that no key can meet: 0 (keys are >= 2^40).
+unsigned long long key_threshold(double gamma) {
+    if (!(gamma > 0.0)) return ~0ull;
+    if (std::isinf(gamma)) return 0ull;
+    int e = 0;
+    const double f = std::frexp(gamma, &e);  // gamma = f * 2^e, f in [0.5, 1)
+    const unsigned long long M = static_cast<unsigned long long>(std::ldexp(f, 53));  // exact
+    const int sh = 93 - e;
+    if (sh >= 127) return ~0ull;  // M * key < 2^110 <= 2^sh for every key
+    if (sh <= 0) return 0ull;
+    const unsigned __int128 lim = (static_cast<unsigned __int128>(1) << sh) - 1;
+    const unsigned __int128 q = lim / M;
+    return q > static_cast<unsigned __int128>(~0ull) ? ~0ull : static_cast<unsigned long long>(q);
+}
+
+int commit_impl(tt_handle h, const char* name, const float* logits, int B, int L, int V,
+                const uint8_t* masked, int k, int steps_left, unsigned long long kthr,
+                int32_t* tok, uint8_t* masked_out, void* workspace, size_t workspace_bytes,
+                void* stream) {
+    if (!h) return fail(TT_ERR_INVALID_ARG, "%s: handle is NULL", name);
+    if (B < 0) return fail(TT_ERR_INVALID_ARG, "%s: B=%d < 0", name, B);
     if (L < 1 || L > tt::kCommitMaxL)
-        return fail(TT_ERR_UNSUPPORTED, "tt_commit: L=%d outside [1, %d]", L, tt::kCommitMaxL);
-    if (k < 1) return fail(TT_ERR_INVALID_ARG, "tt_commit: k=%d < 1", k);
+        return fail(TT_ERR_UNSUPPORTED, "%s: L=%d outside [1, %d]", name, L, tt::kCommitMaxL);
     if (V < 4 || V % 4 || V > tt::kCommitCluster * tt::kCommitSliceMax)
-        return fail(TT_ERR_UNSUPPORTED, "tt_commit: V=%d must be a multiple of 4 in [4, %d]", V,
+        return fail(TT_ERR_UNSUPPORTED, "%s: V=%d must be a multiple of 4 in [4, %d]", name, V,
                     tt::kCommitCluster * tt::kCommitSliceMax);
-    if (static_cast<long>(B) * L * tt::kCommitCluster > 0x7fffffffL)
-        return fail(TT_ERR_UNSUPPORTED, "tt_commit: B*L too large");
+    if (static_cast<long>(B) * L > 0x7fffffffL / tt::kCommitCluster)
+        return fail(TT_ERR_UNSUPPORTED, "%s: B*L too large", name);
     if (B == 0) return TT_OK;
     if (!logits || !masked || !tok || !masked_out)
-        return fail(TT_ERR_INVALID_ARG, "tt_commit: a tensor pointer is NULL");
-    if (!aligned16(logits)) return fail(TT_ERR_INVALID_ARG, "tt_commit: logits must be 16-byte aligned");
-    if (!aligned16(tok)) return fail(TT_ERR_INVALID_ARG, "tt_commit: tok must be 16-byte aligned");
+        return fail(TT_ERR_INVALID_ARG, "%s: a tensor pointer is NULL", name);
+    if (!aligned16(logits)) return fail(TT_ERR_INVALID_ARG, "%s: logits must be 16-byte aligned", name);
+    if (!aligned16(tok)) return fail(TT_ERR_INVALID_ARG, "%s: tok must be 16-byte aligned", name);
     const size_t need = tt_commit_workspace_bytes(B, L);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return fail(TT_ERR_WORKSPACE, "tt_commit: needs %zu workspace bytes (256-byte aligned)", need);
+        return fail(TT_ERR_WORKSPACE, "%s: needs %zu workspace bytes (256-byte aligned)", name, need);
     DeviceGuard g(h->device);
     if (!g.ok()) return fail(TT_ERR_CUDA, "cannot select device %d", h->device);
     tt::CommitParams p;
     p.logits = logits;
     p.B = B; p.L = L; p.V = V; p.k = k;
+    p.steps_left = steps_left;
+    p.kthr = kthr;
     p.slice = (((V + tt::kCommitCluster - 1) / tt::kCommitCluster) + 3) & ~3;
     p.masked = masked;
     p.tok = tok;
@@ -360,6 +385,29 @@ int tt_commit(tt_handle h, const float* logits, int B, int L, int V, const uint8
     cudaError_t e = tt::launch_commit(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "commit launch");
     return TT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tt_commit(tt_handle h, const float* logits, int B, int L, int V, const uint8_t* masked, int k,
+              int32_t* tok, uint8_t* masked_out, void* workspace, size_t workspace_bytes,
+              void* stream) {
+    if (k < 1) return fail(TT_ERR_INVALID_ARG, "tt_commit: k=%d < 1", k);
+    return commit_impl(h, "tt_commit", logits, B, L, V, masked, k, 0, 0ull, tok, masked_out,
+                       workspace, workspace_bytes, stream);
+}
+
+int tt_commit_threshold(tt_handle h, const float* logits, int B, int L, int V,
+                        const uint8_t* masked, double gamma, int steps_left, int32_t* tok,
+                        uint8_t* masked_out, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    if (steps_left < 1)
+        return fail(TT_ERR_INVALID_ARG, "tt_commit_threshold: steps_left=%d < 1", steps_left);
+    if (std::isnan(gamma)) return fail(TT_ERR_INVALID_ARG, "tt_commit_threshold: gamma is NaN");
+    return commit_impl(h, "tt_commit_threshold", logits, B, L, V, masked, 1, steps_left,
+                       key_threshold(gamma), tok, masked_out, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -43,6 +43,11 @@ cudaError_t launch_attn_merge(const AttnParams& p, int D, cudaStream_t s);
 struct CommitParams {
     const float* logits;
     int B, L, V, k;
+    // Threshold mode (steps_left >= 1): a block commits its masked rows with
+    // key <= kthr (confidence above gamma) and at least ceil(n / steps_left) of
+    // its n masked rows; k is unused. steps_left == 0: a fixed budget of k.
+    int steps_left;
+    unsigned long long kthr;
     int slice;  // logits per CTA of a row's cluster (multiple of 4)
     const uint8_t* masked;
     int32_t* tok;

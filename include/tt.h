@@ -153,6 +153,27 @@ int tt_commit(tt_handle handle, const float* logits, int B, int L, int V, const 
               void* stream);
 
 /* ------------------------------------------------------------------------
+ * Unmask / commit with a confidence threshold -- Section 2.2, Algorithm 2,
+ * ConfidenceSample read as: at denoising step r of T, a block commits every
+ * still-masked position whose confidence exceeds gamma, and never fewer than
+ * ceil(#masked / (T - r + 1)) of its most confident masked positions, so that
+ * the block is complete after T steps (steps_left = T - r + 1; with
+ * steps_left = 1 every masked position commits).
+ * The confidence of row r is 2^40 / key_r (key and prediction as in
+ * tt_commit); "confidence > gamma" is decided exactly as gamma * key_r < 2^40
+ * in integer arithmetic (gamma as the double given). The rows that pass are
+ * the first ones of the (key, row) order, so the committed set is the first
+ * max(#passing, ceil(#masked / steps_left)) masked rows of each block in that
+ * order. gamma <= 0 commits every masked row; gamma >= 1 reduces to the floor.
+ * Arguments, layouts, workspace and errors as tt_commit; gamma must not be NaN
+ * and steps_left must be >= 1.
+ * ------------------------------------------------------------------------ */
+int tt_commit_threshold(tt_handle handle, const float* logits, int B, int L, int V,
+                        const uint8_t* masked, double gamma, int steps_left, int32_t* tok,
+                        uint8_t* masked_out, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* ------------------------------------------------------------------------
  * Allocation-free commit. The paper has no counterpart of this entry point:
  * it is the same step as tt_commit, for callers that cannot allocate device
  * memory -- a serving engine that reserves all of HBM for its own pool at

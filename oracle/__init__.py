@@ -60,6 +60,12 @@ def _load():
             lib.tt_oracle_commit.restype = ctypes.c_int
             lib.tt_oracle_commit.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_long, P,
                                              ctypes.c_int, P, P, P, P, ctypes.c_int]
+            lib.tt_oracle_conf_above.restype = ctypes.c_int
+            lib.tt_oracle_conf_above.argtypes = [ctypes.c_uint64, ctypes.c_double]
+            lib.tt_oracle_commit_threshold.restype = ctypes.c_int
+            lib.tt_oracle_commit_threshold.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_long,
+                                                       P, ctypes.c_double, ctypes.c_int, P, P, P, P,
+                                                       ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -144,4 +150,32 @@ def commit(logits, B, L, masked, k, tok, threads=0):
                               _ptr(m_out), _ptr(keys), _ptr(args), int(threads))
     if rc != 0:
         raise ValueError("oracle commit: invalid arguments")
+    return tok_out, m_out, keys, args
+
+
+def conf_above(key: int, gamma: float) -> bool:
+    """Whether a row with canonical key `key` has confidence 2^40/key > gamma (exact)."""
+    return bool(_load().tt_oracle_conf_above(int(key), float(gamma)))
+
+
+def commit_threshold(logits, B, L, masked, gamma, steps_left, tok, threads=0):
+    """One threshold unmasking step (Algorithm 2): per block, every masked row
+    with confidence > gamma, and at least ceil(#masked / steps_left) rows.
+
+    Returns (tok_out, masked_out, keys, args) like ``commit``.
+    """
+    lib = _load()
+    logits = _c(logits, np.float32)
+    R, V = logits.shape
+    assert R == B * L
+    m_in = _c(masked, np.uint8).copy()
+    tok_out = _c(tok, np.int32).copy()
+    m_out = np.empty(R, np.uint8)
+    keys = np.zeros(R, np.uint64)
+    args = np.zeros(R, np.int32)
+    rc = lib.tt_oracle_commit_threshold(_ptr(logits), B, L, V, _ptr(m_in), float(gamma),
+                                        int(steps_left), _ptr(tok_out), _ptr(m_out), _ptr(keys),
+                                        _ptr(args), int(threads))
+    if rc != 0:
+        raise ValueError("oracle commit_threshold: invalid arguments")
     return tok_out, m_out, keys, args

@@ -152,3 +152,79 @@ int tt_oracle_commit(const float* logits, int B, int L, long V, const uint8_t* m
     free(key); free(arg); free(m_in); free(buf);
     return 0;
 }
+
+/*
+ * Confidence above a threshold (Section 2.2, Algorithm 2, "predictions above
+ * gamma are committed"): confidence = 2^40 / key, so conf > gamma is
+ * gamma * key < 2^40, decided in exact arithmetic. gamma = f * 2^e with f in
+ * [0.5, 1), and m = f * 2^53 is an integer, so the test is
+ * m * key < 2^(93 - e) on 128-bit integers.
+ */
+int tt_oracle_conf_above(uint64_t key, double gamma) {
+    if (!(gamma > 0.0)) return 1;   /* every confidence is positive */
+    if (isinf(gamma)) return 0;
+    int e;
+    const double f = frexp(gamma, &e);
+    const unsigned __int128 m = (unsigned __int128)(uint64_t)ldexp(f, 53);
+    const int sh = 93 - e;
+    if (sh >= 127) return 1;        /* m * key < 2^110 <= 2^sh */
+    if (sh <= 0) return 0;
+    return m * (unsigned __int128)key < ((unsigned __int128)1 << sh);
+}
+
+/*
+ * One step of threshold unmasking: per block, commit every masked row whose
+ * confidence exceeds gamma, and at least ceil(n / steps_left) of the n masked
+ * rows (the most confident first), so that a block is complete after
+ * steps_left more steps. Rows are ranked by (key ascending, row ascending).
+ * Same arguments and results as tt_oracle_commit otherwise.
+ */
+int tt_oracle_commit_threshold(const float* logits, int B, int L, long V, const uint8_t* masked,
+                               double gamma, int steps_left, int32_t* tok, uint8_t* masked_out,
+                               uint64_t* keys_out, int32_t* args_out, int nthreads) {
+    if (B < 0 || L < 0 || V < 1 || steps_left < 1 || isnan(gamma)) return -1;
+    const long R = (long)B * L;
+    uint64_t* key = (uint64_t*)malloc(sizeof(uint64_t) * (R ? R : 1));
+    int32_t* arg = (int32_t*)malloc(sizeof(int32_t) * (R ? R : 1));
+    uint8_t* m_in = (uint8_t*)malloc(R ? R : 1);
+    keyed_row* buf = (keyed_row*)malloc(sizeof(keyed_row) * (L ? L : 1));
+    if (!key || !arg || !m_in || !buf) { free(key); free(arg); free(m_in); free(buf); return -1; }
+    memcpy(m_in, masked, R);
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long r = 0; r < R; ++r)
+        if (m_in[r]) tt_oracle_row_key(logits + (size_t)r * V, V, &arg[r], &key[r]);
+
+    for (int b = 0; b < B; ++b) {
+        int n = 0, above = 0;
+        for (int i = 0; i < L; ++i) {
+            const long r = (long)b * L + i;
+            if (m_in[r]) {
+                buf[n].key = key[r];
+                buf[n].row = i;
+                ++n;
+                above += tt_oracle_conf_above(key[r], gamma);
+            }
+        }
+        qsort(buf, n, sizeof(keyed_row), cmp_keyed);
+        for (int i = 0; i < L; ++i) masked_out[(long)b * L + i] = m_in[(long)b * L + i];
+        const int floor_k = (n + steps_left - 1) / steps_left;
+        const int c = above > floor_k ? above : floor_k;
+        for (int j = 0; j < c && j < n; ++j) {
+            const long r = (long)b * L + buf[j].row;
+            tok[r] = arg[r];
+            masked_out[r] = 0;
+        }
+    }
+    for (long r = 0; r < R; ++r)
+        if (m_in[r]) {
+            if (keys_out) keys_out[r] = key[r];
+            if (args_out) args_out[r] = arg[r];
+        }
+    free(key); free(arg); free(m_in); free(buf);
+    return 0;
+}
