@@ -5,6 +5,8 @@ A step is one pass of the whole hot path over one batch: tt_block_attn (one
 denoiser layer's block attention over the context KV cache, "Nemotron-Labs-
 TwoTower" Section 2.1 Eq. 1) followed by tt_commit (one confidence-unmasking
 step, Section 2.2 Algorithm 2, k commits per block) on a fully masked block.
+For a generation schedule (b4_gen8k_32x256: 32 blocks, the context growing
+by one block each time) a step is that pair of calls for every block.
 
 Metric: denoised block-tokens per second per layer-step (B*L tokens per step),
 plus each call's fraction of its roofline (tensor TFLOP/s for attention, HBM
@@ -173,13 +175,20 @@ class ClockSampler:
                 "reasons": sorted(self.reasons), "samples": len(self.samples)}
 
 
-def config_of(w, ctx):
+def config_of(w, inps):
+    ctx = inps[0].ctx_len
+    if len(inps) > 1:
+        lens = [int(i.ctx_len[0]) for i in inps]
+        ctx_desc = f"{lens[0]}..{lens[-1]} over {len(inps)} calls (one per generated block)"
+    elif len(set(ctx.tolist())) == 1:
+        ctx_desc = int(ctx[0])
+    else:
+        ctx_desc = f"{int(ctx.min())}..{int(ctx.max())} ragged, sum {int(ctx.sum())}"
     c = {"workload": w.name, "B": w.B, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-         "ctx_len": (int(ctx[0]) if len(set(ctx.tolist())) == 1
-                     else f"{int(ctx.min())}..{int(ctx.max())} ragged, sum {int(ctx.sum())}"),
-         "ctx_cap": w.ctx_cap, "V": w.V, "k": w.k, "layer_calls_per_step": 1,
+         "ctx_len": ctx_desc, "ctx_cap": w.ctx_cap, "V": w.V, "k": w.k,
+         "layer_calls_per_step": len(inps),
          "commit_state": "fully masked block (first denoising step)",
-         "l2": "flushed between steps, outside the timed events: a 256 MiB write, then a "
+         "l2": "flushed before every call, outside the timed events: a 256 MiB write, then a "
                "read of the same buffer so that no dirty line is left to be written back "
                "inside the timed region"}
     return c
@@ -187,7 +196,7 @@ def config_of(w, ctx):
 
 # ---------------------------------------------------------------- CPU oracle arm
 def cpu_oracle_step(w, inp, cinp, seqs, threads=0):
-    """The oracle on whole sequences `seqs`: attention rows + commit of their blocks."""
+    """The oracle on whole sequences `seqs` of one call: attention rows + commit of their blocks."""
     import oracle
     rows = np.array([[b, l, h] for b in seqs for l in range(w.L) for h in range(w.Hq)], np.int32)
     oracle.block_attn(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx, inp.v_ctx, inp.ctx_len,
@@ -199,44 +208,56 @@ def cpu_oracle_step(w, inp, cinp, seqs, threads=0):
     return len(seqs) * w.L
 
 
-def cpu_baseline(w, inp, cinp, budget_s=12.0):
+def sample_calls(inps, n=4):
+    """Calls spread over a schedule (all of them when there are few)."""
+    if len(inps) <= n:
+        return list(range(len(inps)))
+    return sorted({round(i * (len(inps) - 1) / (n - 1)) for i in range(n)})
+
+
+def cpu_baseline(w, inps, cinp, budget_s=12.0):
     """The oracle as it stands, on all host cores, for about `budget_s` seconds:
-    whole sequences of the same workload (all heads, the block's commit)."""
+    whole sequences of the same workload (all heads, the block's commit); for
+    a schedule, sequences of calls spread over it."""
     cores = os.cpu_count() or 1
+    calls = sample_calls(inps)
     t0 = time.perf_counter()
-    cpu_oracle_step(w, inp, cinp, [0])  # calibration (also warms the caches)
+    cpu_oracle_step(w, inps[calls[0]], cinp, [0])  # calibration (also warms the caches)
     per_seq = time.perf_counter() - t0
-    n = max(1, int(budget_s / max(per_seq, 1e-6)))
-    seqs = [i % w.B for i in range(n)]
+    n = max(len(calls), int(budget_s / max(per_seq, 1e-6)))
     t1 = time.perf_counter()
-    done = cpu_oracle_step(w, inp, cinp, seqs)
+    done = 0
+    for i in range(n):
+        done += cpu_oracle_step(w, inps[calls[i % len(calls)]], cinp, [i % w.B])
     dt = time.perf_counter() - t1
+    what = "" if len(inps) == 1 else f" over calls {calls} of the {len(inps)}-call schedule"
     return {"value": done / dt, "unit": "block-tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} sequences of {w.L} block tokens (cycling over the batch of {w.B}; "
-                      f"all {w.Hq} heads, fp64 attention loops + scalar commit), {dt:.2f} s"}
+            "sample": f"{n} sequences of {w.L} block tokens{what} (cycling over the batch of "
+                      f"{w.B}; all {w.Hq} heads, fp64 attention loops + scalar commit), {dt:.2f} s"}
 
 
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    inp = wl.attn_inputs(w, seed=0)
+    inps = attn_calls(w, seed=0)
     cinp = wl.commit_inputs(w, seed=0)
+    calls = sample_calls(inps)
     cores = os.cpu_count() or 1
-    # each step: one whole sequence (cycling), so K steps stay within minutes
+    # each step: one whole sequence of one call (cycling), so K steps stay within minutes
     for i in range(args.warmup):
-        cpu_oracle_step(w, inp, cinp, [i % w.B])
+        cpu_oracle_step(w, inps[calls[i % len(calls)]], cinp, [i % w.B])
     t0 = time.perf_counter()
     tokens = 0
     for i in range(args.steps):
-        tokens += cpu_oracle_step(w, inp, cinp, [i % w.B])
+        tokens += cpu_oracle_step(w, inps[calls[i % len(calls)]], cinp, [i % w.B])
     dt = time.perf_counter() - t0
     v = tokens / dt
     line = {"metric": "denoised block-tokens/s per layer-step", "value": v,
             "unit": "block-tokens/s", "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded Philox normals)", "config": config_of(w, inp.ctx_len),
+            "data": "synthetic (seeded Philox normals)", "config": config_of(w, inps),
             "cpu_baseline": {"value": v, "unit": "block-tokens/s", "cores": cores,
                              "kind": "oracle",
                              "sample": f"one sequence per step ({w.L} block tokens, all heads)"},
@@ -247,6 +268,24 @@ def run_reference(args, w):
 
 
 # ---------------------------------------------------------------- GPU arm
+def attn_calls(w, seed):
+    """The attention calls of one step: (AttnInputs-like dict of numpy arrays, ctx_len).
+
+    A single-call workload has one; a schedule (one call per generated block,
+    the context growing) has one per block, all reading one context cache
+    (filled for the longest context; shorter calls see a prefix of it)."""
+    if not w.ctx_schedule:
+        inp = wl.attn_inputs(w, seed=seed)
+        return [inp]
+    last = wl.attn_inputs(w, seed=seed, call=len(w.ctx_schedule) - 1)
+    calls = []
+    for j in range(len(w.ctx_schedule)):
+        q, kb, vb = wl.block_inputs(w, seed=seed, call=j)
+        calls.append(wl.AttnInputs(q, kb, vb, last.k_ctx, last.v_ctx, wl.ctx_lens(w, seed, j),
+                                   last.scale))
+    return calls
+
+
 def run_gpu(args, w):
     import torch
     import block_diffusion_decoding_attn_b300 as tt
@@ -268,19 +307,29 @@ def run_gpu(args, w):
     h = tt.handle(local)
 
     # inputs resident in HBM before timing (each rank its own batch)
-    inp = wl.attn_inputs(w, seed=rank)
+    inps = attn_calls(w, seed=rank)
     cinp = wl.commit_inputs(w, seed=rank)
-    A = wl.attn_tensors(inp, dev, pin=True)
+    cache = wl.attn_tensors(inps[-1], dev, pin=True)  # context cache shared by all calls
+    As = []
+    for inp in inps:
+        if inp is inps[-1]:
+            As.append(cache)
+            continue
+        t = wl.attn_tensors(wl.AttnInputs(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx[:0], inp.v_ctx[:0],
+                                          inp.ctx_len, inp.scale), dev, pin=True)
+        t["k_ctx"], t["v_ctx"] = cache["k_ctx"], cache["v_ctx"]
+        As.append(t)
     Cm = wl.commit_tensors(cinp, dev, pin=True)
-    out = torch.empty_like(A["q"])
+    out = torch.empty_like(As[0]["q"])
     m_out = torch.empty_like(Cm["masked"])
-    desc = tt.attn_desc(A["q"], A["k_ctx"])
+    desc = tt.attn_desc(As[0]["q"], As[0]["k_ctx"])
     ws_a_n = tt.block_attn_workspace_bytes(desc, h)
     ws_a = torch.empty(max(ws_a_n, 256), dtype=torch.uint8, device=dev)
     ws_c = torch.zeros(max(tt.commit_workspace_bytes(w.B, w.L), 256), dtype=torch.uint8,
                        device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_sum = torch.empty((), dtype=torch.int64, device=dev)
+    ncalls = len(As)
 
     def flush_l2():
         # Evicts the step's inputs from the 126 MB L2. The write alone would
@@ -291,38 +340,43 @@ def run_gpu(args, w):
         flush_sum.copy_(flush.view(torch.int64).sum())
 
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 1 + (1 if ws_a_n > 0 else 0) + 1  # attention (+ split merge) + commit
+    # per call: attention (+ split merge) + commit
+    launches_per_step = ncalls * (1 + (1 if ws_a_n > 0 else 0) + 1)
 
-    def step():
+    def attention(A):
         tt.block_attn(A["q"], A["k_blk"], A["v_blk"], A["k_ctx"], A["v_ctx"], A["ctx_len"],
                       out=out, workspace=ws_a, h=h, stream=stream)
+
+    def commit():
         tt.commit(Cm["logits"], w.B, w.L, Cm["masked"], w.k, Cm["tok"], masked_out=m_out,
                   workspace=ws_c, h=h, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
-        flush_l2()
-        step()
+        for A in As:
+            flush_l2()
+            attention(A)
+            commit()
     torch.cuda.synchronize()
     if h.get_error():
         raise RuntimeError("device status set during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(ncalls)]
+          for _ in range(K)]
     with ClockSampler(local) as clk:
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for i in range(K):
-            flush_l2()
-            e0, e1, e2 = ev[i]
-            e0.record(stream)
-            tt.block_attn(A["q"], A["k_blk"], A["v_blk"], A["k_ctx"], A["v_ctx"], A["ctx_len"],
-                          out=out, workspace=ws_a, h=h, stream=stream)
-            e1.record(stream)
-            tt.commit(Cm["logits"], w.B, w.L, Cm["masked"], w.k, Cm["tok"], masked_out=m_out,
-                      workspace=ws_c, h=h, stream=stream)
-            e2.record(stream)
+            for j, A in enumerate(As):
+                flush_l2()  # every call starts from a cold L2
+                e0, e1, e2 = ev[i][j]
+                e0.record(stream)
+                attention(A)
+                e1.record(stream)
+                commit()
+                e2.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         if dist:
@@ -330,37 +384,50 @@ def run_gpu(args, w):
     st = h.get_error()
     if st:
         raise RuntimeError(f"device status {st} during the timed region")
-    t_attn = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    t_comm = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    t_attn = [sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for j in range(ncalls)) for i in range(K)]
+    t_comm = [sum(ev[i][j][1].elapsed_time(ev[i][j][2]) for j in range(ncalls)) for i in range(K)]
     ms_step = (sum(t_attn) + sum(t_comm)) / K
     if dist:
         t = torch.tensor([ms_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step = float(t.item())
-    tokens = w.B * w.L * world
+    tokens = w.B * w.L * ncalls * world
     value = tokens / (ms_step * 1e-3)
 
-    # end to end through the public API: host (pinned) buffers in, results out
-    host_in = {k: v.cpu().pin_memory() for k, v in list(A.items()) + list(Cm.items())}
+    # End to end through the public API: host (pinned) buffers in, results
+    # out. Per step: the context cache once, every call's block tensors and
+    # the commit inputs; the attention output, ids and mask of every call back.
+    host_cache = {k: cache[k].cpu().pin_memory() for k in ("k_ctx", "v_ctx")}
+    host_calls = [{k: A[k].cpu().pin_memory() for k in ("q", "k_blk", "v_blk", "ctx_len")}
+                  for A in As]
+    host_commit = {k: v.cpu().pin_memory() for k, v in Cm.items()}
     host_out = {"out": torch.empty_like(out, device="cpu").pin_memory(),
                 "tok": torch.empty_like(Cm["tok"], device="cpu").pin_memory(),
                 "masked": torch.empty_like(m_out, device="cpu").pin_memory()}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
-    Ke = max(3, min(K, 20))
+    dev_cache = {k: torch.empty_like(v, device=dev) for k, v in host_cache.items()}
+    dev_call = {k: torch.empty_like(v, device=dev) for k, v in host_calls[0].items()}
+    dev_commit = {k: torch.empty_like(v, device=dev) for k, v in host_commit.items()}
+    nbytes = lambda d: sum(v.numel() * v.element_size() for v in d.values())  # noqa: E731
+    h2d = nbytes(host_cache) + sum(nbytes(c) for c in host_calls) + ncalls * nbytes(host_commit)
+    d2h = ncalls * nbytes(host_out)
+    Ke = max(3, min(K, 20 if ncalls == 1 else 3))
 
     def e2e_step():
-        for k, v in host_in.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        tt.block_attn(dev_in["q"], dev_in["k_blk"], dev_in["v_blk"], dev_in["k_ctx"],
-                      dev_in["v_ctx"], dev_in["ctx_len"], out=out, workspace=ws_a, h=h,
-                      stream=stream)
-        tt.commit(dev_in["logits"], w.B, w.L, dev_in["masked"], w.k, dev_in["tok"],
-                  masked_out=m_out, workspace=ws_c, h=h, stream=stream)
-        host_out["out"].copy_(out, non_blocking=True)
-        host_out["tok"].copy_(dev_in["tok"], non_blocking=True)
-        host_out["masked"].copy_(m_out, non_blocking=True)
+        for k, v in host_cache.items():
+            dev_cache[k].copy_(v, non_blocking=True)
+        for hc in host_calls:
+            for k, v in hc.items():
+                dev_call[k].copy_(v, non_blocking=True)
+            for k, v in host_commit.items():
+                dev_commit[k].copy_(v, non_blocking=True)
+            tt.block_attn(dev_call["q"], dev_call["k_blk"], dev_call["v_blk"], dev_cache["k_ctx"],
+                          dev_cache["v_ctx"], dev_call["ctx_len"], out=out, workspace=ws_a, h=h,
+                          stream=stream)
+            tt.commit(dev_commit["logits"], w.B, w.L, dev_commit["masked"], w.k,
+                      dev_commit["tok"], masked_out=m_out, workspace=ws_c, h=h, stream=stream)
+            host_out["out"].copy_(out, non_blocking=True)
+            host_out["tok"].copy_(dev_commit["tok"], non_blocking=True)
+            host_out["masked"].copy_(m_out, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -381,22 +448,24 @@ def run_gpu(args, w):
         return 0
 
     peaks = load_peaks()
-    a_ms, c_ms = statistics.mean(t_attn), statistics.mean(t_comm)
-    fl, by_a = attn_flops(w, inp.ctx_len), attn_bytes(w, inp.ctx_len)
+    a_ms, c_ms = statistics.mean(t_attn) / ncalls, statistics.mean(t_comm) / ncalls  # per call
+    fl = sum(attn_flops(w, inp.ctx_len) for inp in inps) / ncalls
+    by_a = sum(attn_bytes(w, inp.ctx_len) for inp in inps) / ncalls
     by_c = commit_bytes(w, int(cinp.masked.sum()))
     attn_tf = fl / (a_ms * 1e-3) / 1e12
     comm_gbs = by_c / (c_ms * 1e-3) / 1e9
+    per = "per call" if ncalls == 1 else f"per call, mean over the {ncalls} calls of a step"
     roof_attn = {"bound": "tensor", "achieved": attn_tf, "peak": peaks["bf16_tflops"],
                  "unit": "TFLOP/s", "frac": attn_tf / peaks["bf16_tflops"],
                  "traffic": profiled_traffic("block_attn", w.name),
                  "kernel": "tt_block_attn call (attention kernel + split merge)",
-                 "algorithmic": f"{fl:.4g} FLOP, {by_a:.4g} B per call",
+                 "algorithmic": f"{fl:.4g} FLOP, {by_a:.4g} B {per}",
                  "ms": a_ms, "peak_source": peaks["source"] + " burst"}
     roof_comm = {"bound": "hbm", "achieved": comm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                  "frac": comm_gbs / peaks["hbm_gbs"],
                  "traffic": profiled_traffic("commit", w.name),
                  "kernel": "tt_commit call (row reduction + top-k select)",
-                 "algorithmic": f"{by_c:.4g} B per call", "ms": c_ms,
+                 "algorithmic": f"{by_c:.4g} B {per}", "ms": c_ms,
                  "peak_source": peaks["source"]}
     dom = roof_attn if a_ms >= c_ms else roof_comm
     line = {
@@ -405,7 +474,7 @@ def run_gpu(args, w):
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 (attention, fp32 accumulate) / f32 (commit)",
         "data": "synthetic (seeded Philox normals; inputs resident in HBM)",
-        "config": config_of(w, inp.ctx_len),
+        "config": config_of(w, inps),
         "roofline": dom,
         "kernels": {"attention": roof_attn, "commit": roof_comm},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "block-tokens/s",
@@ -416,7 +485,7 @@ def run_gpu(args, w):
         "wall_s_timed_region": wall,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, inp, cinp)
+        line["cpu_baseline"] = cpu_baseline(w, inps, cinp)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -435,8 +504,6 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     w = wl.WORKLOADS[args.workload]
-    if w.ctx_schedule:
-        raise SystemExit("multi-call schedules are parity cases; bench a single-call workload")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_gpu(args, w)

@@ -192,6 +192,18 @@ def attn_inputs(w: Workload, seed: int = 0, call: int = 0, pad=BF16_NAN) -> Attn
     return AttnInputs(q, kb, vb, kc, vc, cl, 1.0 / math.sqrt(D))
 
 
+def block_inputs(w: Workload, seed: int = 0, call: int = 0):
+    """q, k_blk, v_blk of attention call `call` alone (the draws attn_inputs
+    makes for them), for schedules that share one context cache."""
+    std = w.qk_std if w.qk_std > 0 else 1.0 / math.sqrt(w.D)
+    B, L, Hq, Hkv, D = w.B, w.L, w.Hq, w.Hkv, w.D
+    sub = call * 16
+    q = _fill_normal(B * L * Hq * D, std, seed, w.wid, _T_Q + sub, True).reshape(B, L, Hq, D)
+    kb = _fill_normal(B * L * Hkv * D, std, seed, w.wid, _T_KBLK + sub, True).reshape(B, L, Hkv, D)
+    vb = _fill_normal(B * L * Hkv * D, std, seed, w.wid, _T_VBLK + sub, True).reshape(B, L, Hkv, D)
+    return q, kb, vb
+
+
 @dataclasses.dataclass
 class CommitInputs:
     logits: np.ndarray  # float32 [B*L][V]
