@@ -268,6 +268,23 @@ def run_reference(args, w):
 
 
 # ---------------------------------------------------------------- GPU arm
+def max_over_ranks(ms, dist=None):
+    """The step time of the whole job: the max of the ranks' times (every rank
+    gets it). Tensors live on the process group's device (CUDA under NCCL)."""
+    if dist is None:
+        return ms
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def tokens_per_step(w, ncalls, world):
+    """Block tokens of one step over the whole job (each rank its own batch)."""
+    return w.B * w.L * ncalls * world
+
+
 def attn_calls(w, seed):
     """The attention calls of one step: (AttnInputs-like dict of numpy arrays, ctx_len).
 
@@ -386,12 +403,8 @@ def run_gpu(args, w):
         raise RuntimeError(f"device status {st} during the timed region")
     t_attn = [sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for j in range(ncalls)) for i in range(K)]
     t_comm = [sum(ev[i][j][1].elapsed_time(ev[i][j][2]) for j in range(ncalls)) for i in range(K)]
-    ms_step = (sum(t_attn) + sum(t_comm)) / K
-    if dist:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    tokens = w.B * w.L * ncalls * world
+    ms_step = max_over_ranks((sum(t_attn) + sum(t_comm)) / K, dist)
+    tokens = tokens_per_step(w, ncalls, world)
     value = tokens / (ms_step * 1e-3)
 
     # End to end through the public API: host (pinned) buffers in, results
@@ -437,11 +450,7 @@ def run_gpu(args, w):
     for _ in range(Ke):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - te0) / Ke * 1e3
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks((time.perf_counter() - te0) / Ke * 1e3, dist)
 
     if rank != 0:
         dist.destroy_process_group() if dist else None
