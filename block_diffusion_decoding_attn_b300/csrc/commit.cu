@@ -81,15 +81,15 @@ constexpr int kRowCols = kSliceMax / 128;           // 256 TMEM columns per row 
 constexpr int kP1Warps = 8;               // pass 1: warps 0-7 (two per TMEM lane quarter)
 constexpr int kP2Warps = 8;               // pass 2: warps 8-15
 constexpr int kP1Threads = kP1Warps * 32;
-constexpr int kP2Threads = kP2Warps * 32;
 constexpr int kProducerWarp = kP1Warps + kP2Warps;  // warp 16
 constexpr int kCollectorWarp = kProducerWarp + 1;   // warp 17 (CTA 0 only)
+constexpr int kAmSenderWarp = kCollectorWarp + 1;   // warp 18: slice results -> the cluster
+constexpr int kSumSenderWarp = kAmSenderWarp + 1;   // warp 19: partial keys -> CTA 0
 constexpr int kP1PerChunk = kChunk / kP1Threads;    // logits per pass-1 thread per chunk
 constexpr int kP2Cols = kRowCols / (kP2Warps / 4);  // TMEM columns per pass-2 thread
-constexpr int kThreads = (kCollectorWarp + 1) * 32;
+constexpr int kThreads = (kSumSenderWarp + 1) * 32;
 constexpr int kXchg = 8;                  // exchange slots (rows in flight in the cluster)
 constexpr int kSelChunk = 2048;           // keys staged per selection pass
-constexpr uint32_t kBarP1 = 1, kBarP2 = 2;  // named barriers of the two warp roles
 static_assert(kSliceMax == kCommitSliceMax, "slice per CTA");
 static_assert(2 * kRowCols == 512, "two row slots fill the TMEM");
 
@@ -186,16 +186,19 @@ struct CommitShared {
     uint64_t full[kSlots];      // producer -> pass 1: chunk landed
     uint64_t empty[kSlots];     // pass 1 -> producer: slot free (one arrival per pass-1 warp)
     uint64_t tfree[2];          // pass 2 -> pass 1: TMEM row slot free (one arrival per pass-2 warp)
+    uint64_t p1_done[kXchg];    // pass 1 -> slice sender: the row's per-warp results are written
+    uint64_t p2_done[kXchg];    // pass 2 -> key sender: the row's per-warp partial keys are written
     uint64_t am_bar[kXchg];     // one arrival per CTA: its slice (max, argmax)
     uint64_t sum_bar[kXchg];    // one arrival per CTA at CTA 0: its partial key
     uint64_t col_done[kXchg];   // CTA 0: the collector has finished the row
     unsigned long long am_in[kXchg][kCommitCluster];   // written by the cluster's CTAs
     unsigned long long sum_in[kXchg][kCommitCluster];  // (CTA 0 only)
     int col_arg[kXchg];                                 // (CTA 0) prediction of the row
+    int row_arg[kXchg];                                 // pass 2 -> key sender: prediction
     float smin[2];                                      // slice minimum of each TMEM row slot
-    unsigned long long red_am[kP1Warps];
-    float red_min[kP1Warps];
-    unsigned long long red_sum[kP2Warps];
+    unsigned long long red_am[kXchg][kP1Warps];
+    float red_min[kXchg][kP1Warps];
+    unsigned long long red_sum[kXchg][kP2Warps];
     int total;              // masked rows of this cluster
     int row0;               // first row of this cluster's range
     int wsum[kThreads / 32];  // start-up scan: masked rows per warp
@@ -415,6 +418,8 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
         mbar_init(&sh.tfree[0], kP2Warps);
         mbar_init(&sh.tfree[1], kP2Warps);
         for (int q = 0; q < kXchg; ++q) {
+            mbar_init(&sh.p1_done[q], kP1Warps);
+            mbar_init(&sh.p2_done[q], kP2Warps);
             mbar_init(&sh.am_bar[q], kCommitCluster);
             mbar_init(&sh.sum_bar[q], kCommitCluster);
             mbar_init(&sh.col_done[q], 1);
@@ -579,14 +584,19 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
     } else {
         // ---------------------------------------------------------------- pass 1 / pass 2
         // Rows of the cluster's sequence alternate between the two TMEM row
-        // slots (256 columns each). Pass 1 (warps 0-3) drains a row's chunks
+        // slots (256 columns each). Pass 1 (warps 0-7) drains a row's chunks
         // from the ring into its slot, taking the slice max / first argmax /
-        // min, and sends the result to the cluster; pass 2 (warps 4-11) waits
-        // for the cluster's results of that row, sums its fixed-point terms
-        // from TMEM and frees the slot. So pass 1 of row i + 1 and the
-        // exchange run while pass 2 works on row i. Every named barrier also
-        // ANDs the threads' wait results: a wait that gave up in any thread
-        // ends the loop of all the threads of that role at the same barrier.
+        // min; warp 18 sends the result to the cluster. Pass 2 (warps 8-15)
+        // waits for the cluster's results of that row, sums its fixed-point
+        // terms from TMEM and frees the slot; warp 19 sends the partial key to
+        // CTA 0. So pass 1 of row i + 1 and the exchange run while pass 2
+        // works on row i, and no computing warp waits for a DSMEM send. The
+        // per-warp results of row i go through slot i % kXchg of shared
+        // memory; that slot is written again only kXchg rows later, after
+        // the exchange of those rows (whose CTA-0 side waits for the
+        // collector to finish row i) has consumed it. Every wait is bounded;
+        // a role whose wait gives up leaves its loop, and the others' waits
+        // then give up in turn.
         const int per_row = max(nchunks, 1);  // ring entries per row
         const int total = sh.total;
         bool ok = true;
@@ -601,20 +611,21 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
             const int pt = tid;
             const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
             const int csub = kP1PerChunk * (pt / 128);
-            for (int seq = 0; seq < total; ++seq) {
+            for (int seq = 0; seq < total && ok; ++seq) {
                 const int t = seq & 1;
-                bool good = ok;
-                if (seq >= 2) good = good && mbar_wait(&sh.tfree[t], ((seq >> 1) - 1) & 1, limit);
-                good = __all_sync(0xffffffffu, good);
+                const int q = seq % kXchg;
+                if (seq >= 2) ok = mbar_wait(&sh.tfree[t], ((seq >> 1) - 1) & 1, limit);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
                 tc_fence_after();
                 const uint32_t tb = sh.tmem + lane_off + static_cast<uint32_t>(t * kRowCols + csub);
                 float best = -INFINITY, mn = INFINITY;
                 int be = 0x7fffffff;  // slice element of the first maximum
                 int it = seq * per_row;
-                for (int c = 0; c < per_row && good; ++c, ++it) {
+                for (int c = 0; c < per_row && ok; ++c, ++it) {
                     const int s = it % kSlots;
-                    good = __all_sync(0xffffffffu, mbar_wait(&sh.full[s], (it / kSlots) & 1, limit));
-                    if (!good) break;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&sh.full[s], (it / kSlots) & 1, limit));
+                    if (!ok) break;
                     const float* sl = ring + static_cast<size_t>(s) * kChunk;
                     const int lo = c * kChunk;
                     const int n = cnt - lo;  // logits of this chunk (may exceed kChunk)
@@ -650,42 +661,22 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh.empty[s]);  // this warp is done with the slot
                 }
+                if (!ok) break;
                 unsigned long long am = be < cnt ? enc_argmax(best, v0 + be) : 0ull;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) {
                     am = max(am, shfl_xor64(am, o));
                     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
                 }
+                tc_fence_before();  // the row's TMEM stores (waited on) before the arrival
+                __syncwarp();
                 if (lane == 0) {
-                    sh.red_am[warp] = am;
-                    sh.red_min[warp] = mn;
-                }
-                tc_fence_before();
-                if (!named_bar_and(kBarP1, kP1Threads, good)) { ok = false; break; }
-                if (warp == 0) {
-                    const int q = seq % kXchg;
-                    unsigned long long a = lane < kP1Warps ? sh.red_am[lane] : 0ull;
-                    float mnv = lane < kP1Warps ? sh.red_min[lane] : INFINITY;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        a = max(a, shfl_xor64(a, o));
-                        mnv = fminf(mnv, __shfl_xor_sync(0xffffffffu, mnv, o));
-                    }
-                    bool free = true;
-                    // CTA 0 reuses exchange slot q only once the collector is done with it.
-                    if (rank == 0 && seq >= kXchg && lane == 0)
-                        free = mbar_wait(&sh.col_done[q], ((seq / kXchg) - 1) & 1, limit);
-                    free = __shfl_sync(0xffffffffu, free, 0);
-                    if (!free) ok = false;
-                    if (free && lane < kCommitCluster) {  // lane j sends to CTA j
-                        if (lane == static_cast<int>(rank)) sh.smin[t] = mnv;  // released with it
-                        st_cluster_u64(mapa_shared(smem_u32(&sh.am_in[q][rank]), lane), a);
-                        mbar_arrive_cluster(mapa_shared(smem_u32(&sh.am_bar[q]), lane));
-                    }
-                    __syncwarp();
+                    sh.red_am[q][warp] = am;
+                    sh.red_min[q][warp] = mn;
+                    mbar_arrive(&sh.p1_done[q]);
                 }
             }
-        } else {
+        } else if (warp < kP1Warps + kP2Warps) {
             // ------------------------------------------------------------ pass 2
             // Warp pw reads TMEM lanes 32 (pw % 4) .. + 31 and kP2Cols columns
             // of the slot from kP2Cols * (pw / 4) (inside chunk
@@ -694,11 +685,11 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
             const int c0w = kP2Cols * (pw / 4);
             const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
             const int ncol = c0w / 128 < nchunks ? kP2Cols : 0;
-            for (int seq = 0; seq < total; ++seq) {
+            for (int seq = 0; seq < total && ok; ++seq) {
                 const int t = seq & 1;
                 const int q = seq % kXchg;
-                const bool got = __all_sync(
-                    0xffffffffu, ok && mbar_wait_cluster(&sh.am_bar[q], (seq / kXchg) & 1, limit));
+                ok = __all_sync(0xffffffffu, mbar_wait_cluster(&sh.am_bar[q], (seq / kXchg) & 1, limit));
+                if (!ok) break;
                 tc_fence_after();
                 unsigned long long rm = sh.am_in[q][0];
 #pragma unroll
@@ -712,53 +703,83 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 const f2 m2 = dup(m);
                 unsigned hi = 0, lo = 0;
                 const uint32_t tb = sh.tmem + lane_off + static_cast<uint32_t>(t * kRowCols + c0w);
-                if (got) {
-                    for (int c0 = 0; c0 < ncol; c0 += 32) {
-                        uint32_t rr[32];
-                        tmem_ld32(tb + c0, rr);
-                        if (noclamp) {
+                for (int c0 = 0; c0 < ncol; c0 += 32) {
+                    uint32_t rr[32];
+                    tmem_ld32(tb + c0, rr);
+                    if (noclamp) {
 #pragma unroll
-                            for (int k = 0; k < 32; k += 2)
-                                add_terms(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2),
-                                          hi, lo);
-                        } else {
+                        for (int k = 0; k < 32; k += 2)
+                            add_terms(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2),
+                                      hi, lo);
+                    } else {
 #pragma unroll
-                            for (int k = 0; k < 32; k += 2) {
-                                float d0, d1;
-                                upk(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2),
-                                    d0, d1);
-                                add_terms(pk(fmaxf(d0, -31.0f), fmaxf(d1, -31.0f)), hi, lo);
-                            }
+                        for (int k = 0; k < 32; k += 2) {
+                            float d0, d1;
+                            upk(fsub2(pk(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), m2),
+                                d0, d1);
+                            add_terms(pk(fmaxf(d0, -31.0f), fmaxf(d1, -31.0f)), hi, lo);
                         }
                     }
                 }
+                tc_fence_before();  // the row's TMEM loads (waited on) before the slot is freed
                 hi -= static_cast<unsigned>(ncol) * kMagic43Bits;
                 lo -= static_cast<unsigned>(ncol) * kMagic23Bits;
                 unsigned long long acc = (static_cast<unsigned long long>(hi) << 20) +
                                          static_cast<long long>(static_cast<int>(lo));
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) acc += shfl_xor64(acc, o);
-                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    sh.red_sum[pw] = acc;
-                    if (got) mbar_arrive(&sh.tfree[t]);  // this warp is done with the slot
-                }
-                if (!named_bar_and(kBarP2, kP2Threads, got)) { ok = false; break; }
-                if (pw == 0) {
-                    unsigned long long a = lane < kP2Warps ? sh.red_sum[lane] : 0ull;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) a += shfl_xor64(a, o);
-                    if (lane == 0) {
-                        if (rank == 0) sh.col_arg[q] = dec_index(rm);
-                        st_cluster_u64(mapa_shared(smem_u32(&sh.sum_in[q][rank]), 0), a);
-                        mbar_arrive_cluster(mapa_shared(smem_u32(&sh.sum_bar[q]), 0));
-                    }
-                    __syncwarp();
+                    mbar_arrive(&sh.tfree[t]);  // this warp is done with the slot
+                    sh.red_sum[q][pw] = acc;
+                    if (pw == 0) sh.row_arg[q] = dec_index(rm);
+                    mbar_arrive(&sh.p2_done[q]);
                 }
             }
+        } else if (warp == kAmSenderWarp) {
+            // ------------------------------------------------------------ slice sender
+            for (int seq = 0; seq < total && ok; ++seq) {
+                const int t = seq & 1;
+                const int q = seq % kXchg;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sh.p1_done[q], (seq / kXchg) & 1, limit));
+                if (!ok) break;
+                unsigned long long a = lane < kP1Warps ? sh.red_am[q][lane] : 0ull;
+                float mnv = lane < kP1Warps ? sh.red_min[q][lane] : INFINITY;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    a = max(a, shfl_xor64(a, o));
+                    mnv = fminf(mnv, __shfl_xor_sync(0xffffffffu, mnv, o));
+                }
+                // CTA 0 reuses exchange slot q only once the collector is done with it.
+                if (rank == 0 && seq >= kXchg && lane == 0)
+                    ok = mbar_wait(&sh.col_done[q], ((seq / kXchg) - 1) & 1, limit);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (lane < kCommitCluster) {  // lane j sends to CTA j
+                    if (lane == static_cast<int>(rank)) sh.smin[t] = mnv;  // released with it
+                    st_cluster_u64(mapa_shared(smem_u32(&sh.am_in[q][rank]), lane), a);
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&sh.am_bar[q]), lane));
+                }
+                __syncwarp();
+            }
+        } else {
+            // ------------------------------------------------------------ key sender
+            for (int seq = 0; seq < total && ok; ++seq) {
+                const int q = seq % kXchg;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sh.p2_done[q], (seq / kXchg) & 1, limit));
+                if (!ok) break;
+                unsigned long long a = lane < kP2Warps ? sh.red_sum[q][lane] : 0ull;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) a += shfl_xor64(a, o);
+                if (lane == 0) {
+                    if (rank == 0) sh.col_arg[q] = sh.row_arg[q];
+                    st_cluster_u64(mapa_shared(smem_u32(&sh.sum_in[q][rank]), 0), a);
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&sh.sum_bar[q]), 0));
+                }
+                __syncwarp();
+            }
         }
-        if (!ok && (tid == 0 || tid == kP1Threads)) atomicOr(p.status, kDevWaitTimeout);
+        if (!ok && lane == 0) atomicOr(p.status, kDevWaitTimeout);
         __syncwarp();
     }
     // No CTA leaves while another may still write into its shared memory.
