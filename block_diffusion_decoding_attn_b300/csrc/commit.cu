@@ -178,6 +178,40 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// One group of 32 logits of a pass-1 thread: float4 u8 = 0..7 of the group at
+// ring offsets e0 + 4 * kP1Threads * u8, i.e. in slice order for the thread.
+// Returns the group maximum, folds the group minimum into mn and leaves the
+// raw bits in rr in the same order (TMEM columns 4 u8 + j). kChecked: offsets
+// at or past n (the end of the slice in this chunk) read as -inf.
+template <bool kChecked>
+__device__ __forceinline__ float p1_group(const float* sl, int e0, int n, float& mn,
+                                          uint32_t (&rr)[32]) {
+    float a0 = -INFINITY, a1 = -INFINITY, b0 = mn, b1 = INFINITY;
+#pragma unroll
+    for (int u8 = 0; u8 < 8; ++u8) {
+        const int e = e0 + 4 * kP1Threads * u8;
+        float4 x;
+        if (kChecked && e >= n) x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        else x = *reinterpret_cast<const float4*>(sl + e);
+        a0 = max3(a0, x.x, x.y);
+        a1 = max3(a1, x.z, x.w);
+        b0 = min3(b0, x.x, x.y);
+        b1 = min3(b1, x.z, x.w);
+        rr[4 * u8 + 0] = __float_as_uint(x.x);
+        rr[4 * u8 + 1] = __float_as_uint(x.y);
+        rr[4 * u8 + 2] = __float_as_uint(x.z);
+        rr[4 * u8 + 3] = __float_as_uint(x.w);
+    }
+    mn = fminf(b0, b1);
+    return fmaxf(a0, a1);
+}
+
 __device__ __forceinline__ unsigned long long shfl_xor64(unsigned long long v, int o) {
     return __shfl_xor_sync(0xffffffffu, v, o);
 }
@@ -604,10 +638,15 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
             // ------------------------------------------------------------ pass 1
             // Thread pt writes TMEM lane pt % 128. Chunk c of the row goes to
             // columns 128 c .. 128 c + 127 of the slot, kP1PerChunk of them
-            // from 128 c + kP1PerChunk * (pt / 128) for this thread: float4 u of
-            // the chunk (slice element c * kChunk + 4 * (u * kP1Threads + pt))
-            // in 4 columns from there + 4 u, so the columns run in slice order
-            // for every thread. (Pass 2 only sums, so it reads them in any order.)
+            // from 128 c + kP1PerChunk * (pt / 128) for this thread, in groups
+            // of 32: float4 u of the chunk (slice element c * kChunk +
+            // 4 * (u * kP1Threads + pt)) in 4 columns from there + 4 u, so the
+            // columns run in slice order for every thread. (Pass 2 only sums,
+            // so it reads them in any order.) A thread keeps only its maximum
+            // and the first group that reaches it; once the row is in, the
+            // warp reads those groups back from TMEM (once per distinct group
+            // among the lanes holding the warp maximum) to find the first
+            // element equal to it.
             const int pt = tid;
             const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
             const int csub = kP1PerChunk * (pt / 128);
@@ -620,41 +659,24 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 tc_fence_after();
                 const uint32_t tb = sh.tmem + lane_off + static_cast<uint32_t>(t * kRowCols + csub);
                 float best = -INFINITY, mn = INFINITY;
-                int be = 0x7fffffff;  // slice element of the first maximum
+                int bcol = -1;  // column (from tb) of the group with the thread's first maximum
                 int it = seq * per_row;
                 for (int c = 0; c < per_row && ok; ++c, ++it) {
                     const int s = it % kSlots;
                     ok = __all_sync(0xffffffffu, mbar_wait(&sh.full[s], (it / kSlots) & 1, limit));
                     if (!ok) break;
                     const float* sl = ring + static_cast<size_t>(s) * kChunk;
-                    const int lo = c * kChunk;
-                    const int n = cnt - lo;  // logits of this chunk (may exceed kChunk)
+                    const int n = cnt - c * kChunk;  // logits of this chunk (may exceed kChunk)
+                    const bool whole = n >= kChunk;
 #pragma unroll 1
                     for (int h = 0; h < kP1PerChunk / 32; ++h) {  // groups of 32 logits
                         uint32_t rr[32];
-                        int bu = -1;
-                        float hb = best;
-#pragma unroll
-                        for (int u8 = 0; u8 < 8; ++u8) {
-                            const int u = h * 8 + u8;
-                            const int e = (u * kP1Threads + pt) * 4;
-                            const float4 x = e < n ? *reinterpret_cast<const float4*>(sl + e)
-                                                   : make_float4(-INFINITY, -INFINITY, -INFINITY,
-                                                                 -INFINITY);
-                            const float gmx = fmaxf(max3(x.x, x.y, x.z), x.w);
-                            mn = fminf(mn, fminf(fminf(x.x, x.y), fminf(x.z, x.w)));
-                            if (gmx > hb) { hb = gmx; bu = u; }
-                            rr[4 * u8 + 0] = __float_as_uint(x.x);
-                            rr[4 * u8 + 1] = __float_as_uint(x.y);
-                            rr[4 * u8 + 2] = __float_as_uint(x.z);
-                            rr[4 * u8 + 3] = __float_as_uint(x.w);
-                        }
-                        if (bu >= 0) {  // a new maximum in this group: its first component
-                            const int e = (bu * kP1Threads + pt) * 4;
-                            const float4 x = *reinterpret_cast<const float4*>(sl + e);
-                            const int jj = x.x == hb ? 0 : x.y == hb ? 1 : x.z == hb ? 2 : 3;
+                        const int e0 = 4 * (8 * h * kP1Threads + pt);
+                        const float hb = whole ? p1_group<false>(sl, e0, n, mn, rr)
+                                               : p1_group<true>(sl, e0, n, mn, rr);
+                        if (hb > best) {
                             best = hb;
-                            be = lo + e + jj;
+                            bcol = 128 * c + 32 * h;
                         }
                         tmem_st32(tb + 128 * c + 32 * h, rr);
                     }
@@ -662,12 +684,33 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                     if (lane == 0) mbar_arrive(&sh.empty[s]);  // this warp is done with the slot
                 }
                 if (!ok) break;
-                unsigned long long am = be < cnt ? enc_argmax(best, v0 + be) : 0ull;
+                float wmax = best;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) {
-                    am = max(am, shfl_xor64(am, o));
+                    wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
                     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
                 }
+                // No lane has a group if the warp's logits are all -inf (or NaN):
+                // then the warp offers no candidate (0).
+                unsigned long long am = 0ull;
+                unsigned cand = __ballot_sync(0xffffffffu, bcol >= 0 && best == wmax);
+                while (cand != 0u) {
+                    const int g = __shfl_sync(0xffffffffu, bcol, __ffs(cand) - 1);
+                    uint32_t rr[32];
+                    tmem_ld32(tb + g, rr);  // this thread's own stores (waited on)
+                    if (((cand >> lane) & 1u) && bcol == g) {
+                        int k = 31;
+#pragma unroll
+                        for (int j = 30; j >= 0; --j)
+                            if (__uint_as_float(rr[j]) == wmax) k = j;
+                        const int e = (g / 128) * kChunk +
+                                      4 * ((8 * ((g % 128) / 32) + k / 4) * kP1Threads + pt) + (k & 3);
+                        am = enc_argmax(wmax, v0 + e);
+                    }
+                    cand &= ~__ballot_sync(0xffffffffu, bcol == g);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) am = max(am, shfl_xor64(am, o));
                 tc_fence_before();  // the row's TMEM stores (waited on) before the arrival
                 __syncwarp();
                 if (lane == 0) {
