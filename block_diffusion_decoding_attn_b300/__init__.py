@@ -15,6 +15,9 @@ Entry points mirror the C ABI:
   block per step)
 * :func:`commit_threshold` -> ``tt_commit_threshold`` (Algorithm 2 with a
   confidence threshold gamma and a floor of ceil(#masked / steps_left))
+* :func:`block_attn` with ``causal=True`` -> ``tt_block_attn_causal`` and
+  :func:`kv_append` -> ``tt_kv_append``: the context tower's update after a
+  commit (Section 2.1, Algorithm 1, "update AR context")
 """
 from __future__ import annotations
 
@@ -63,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.tt_block_attn_workspace_bytes.restype = S
             L.tt_block_attn_workspace_bytes.argtypes = [P, ctypes.POINTER(AttnDesc)]
             L.tt_block_attn.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 7 + [P, S, P]
+            L.tt_block_attn_causal.argtypes = L.tt_block_attn.argtypes
+            L.tt_kv_append.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 5 + [P]
             L.tt_commit_workspace_bytes.restype = S
             L.tt_commit_workspace_bytes.argtypes = [I, I]
             L.tt_commit.argtypes = [P, P, I, I, I, P, I, P, P, P, S, P]
@@ -160,11 +165,13 @@ def block_attn_workspace_bytes(desc: AttnDesc, h: Handle | None = None) -> int:
 
 
 def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out=None, scale: float = 0.0,
-               num_splits: int = 0, workspace=None, h: Handle | None = None, stream=None):
+               num_splits: int = 0, workspace=None, h: Handle | None = None, stream=None,
+               causal: bool = False):
     """Block attention, Eq. (1): one softmax per query over [context keys; block keys].
 
     q [B][L][Hq][D], k_blk/v_blk [B][L][Hkv][D], k_ctx/v_ctx [B][Hkv][C_cap][D]
     (torch.bfloat16, CUDA, contiguous); ctx_len [B] int32 on the device.
+    ``causal``: block query l sees block keys 0..l only (tt_block_attn_causal).
     Returns out [B][L][Hq][D] bf16.
     """
     import torch
@@ -183,11 +190,37 @@ def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out=None, scale: float = 
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wsp = _dev_ptr(workspace) if need else ctypes.c_void_p(0)
     wsn = workspace.numel() * workspace.element_size() if need else 0
-    _check(lib().tt_block_attn(h.ptr, ctypes.byref(desc), _dev_ptr(q), _dev_ptr(k_blk),
-                               _dev_ptr(v_blk), _dev_ptr(k_ctx), _dev_ptr(v_ctx),
-                               _dev_ptr(ctx_len), _dev_ptr(out), wsp, wsn,
-                               _stream_ptr(q, stream)), "tt_block_attn")
+    fn = lib().tt_block_attn_causal if causal else lib().tt_block_attn
+    _check(fn(h.ptr, ctypes.byref(desc), _dev_ptr(q), _dev_ptr(k_blk), _dev_ptr(v_blk),
+              _dev_ptr(k_ctx), _dev_ptr(v_ctx), _dev_ptr(ctx_len), _dev_ptr(out), wsp, wsn,
+              _stream_ptr(q, stream)), "tt_block_attn_causal" if causal else "tt_block_attn")
     return out
+
+
+def kv_append(k_blk, v_blk, k_ctx, v_ctx, ctx_len, h: Handle | None = None, stream=None):
+    """Appends the block's K/V to the cache in place and advances ctx_len by L.
+
+    k_blk/v_blk [B][L][Hkv][D], k_ctx/v_ctx [B][Hkv][C_cap][D] (torch.bfloat16,
+    CUDA, contiguous); ctx_len [B] int32 on the device, updated in place. A
+    block that does not fit is skipped and flags TT_DEV_CTX_LEN_RANGE
+    (Handle.get_error).
+    """
+    import torch
+    for name, t in (("k_blk", k_blk), ("v_blk", v_blk), ("k_ctx", k_ctx), ("v_ctx", v_ctx)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    if ctx_len.dtype != torch.int32 or not ctx_len.is_cuda:
+        raise ValueError("ctx_len must be an int32 CUDA tensor")
+    B, L, Hkv, D = k_blk.shape
+    if tuple(v_blk.shape) != (B, L, Hkv, D) or k_ctx.shape[:2] != (B, Hkv) or \
+            k_ctx.shape[3] != D or tuple(v_ctx.shape) != tuple(k_ctx.shape):
+        raise ValueError("kv_append: inconsistent shapes")
+    h = h or handle(k_blk.device.index)
+    desc = AttnDesc(B, L, Hkv, Hkv, D, int(k_ctx.shape[2]), 0.0, 0)
+    _check(lib().tt_kv_append(h.ptr, ctypes.byref(desc), _dev_ptr(k_blk), _dev_ptr(v_blk),
+                              _dev_ptr(k_ctx), _dev_ptr(v_ctx), _dev_ptr(ctx_len),
+                              _stream_ptr(k_blk, stream)), "tt_kv_append")
+    return k_ctx, v_ctx
 
 
 def commit_workspace_bytes(B: int, L: int) -> int:

@@ -3,6 +3,12 @@
 // softmax over [context-tower keys 0..ctx_len-1 of this layer; the block's own
 // L keys], with no mask inside the block and GQA head sharing.
 //
+// The causal variant (p.causal) is the context tower's pass over a committed
+// block (Section 2.1, Algorithm 1, "update AR context"): block query l sees
+// the context and block keys 0..l only. The block tiles are masked per row;
+// a row with no visible key in a split (a block tile past it) keeps m = -inf,
+// a zero sum and zero P there, and the merge gives such a split weight 0.
+//
 // One CTA owns one work unit: (sequence b, KV head, pair of 128-row query
 // tiles, KV split). The G = Hq/Hkv query heads of a KV head are packed with the
 // block positions into the M dimension (row = l*G + g), so each K/V tile staged
@@ -282,6 +288,8 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t ts = tmem + lane_off + (x ? 2u * kTile : 0u);
         const uint32_t to = tmem + lane_off + (x ? 3u * kTile : static_cast<uint32_t>(kTile));
         const float sl2 = p.scale_log2;
+        // block position of this thread's query row (rows past G*L are padding)
+        const int lq = ((2 * pair + x) * kTile + row) / p.G;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
@@ -296,9 +304,12 @@ __global__ void __launch_bounds__(320, 1)
                 for (int c = 0; c < kTile; ++c) s[c] = __uint_as_float(r[c]);
             }
             const KvTile kt = kv_tile(t0 + j, nc, C, p.L);
-            if (kt.valid < kTile) {
+            // keys of this tile the row sees: the tile's keys, and in the causal
+            // variant only block keys up to the row's own position (maybe none)
+            const int lim = (p.causal && !kt.is_ctx) ? min(kt.valid, lq + 1 - kt.base) : kt.valid;
+            if (lim < kTile) {
 #pragma unroll
-                for (int c = 0; c < kTile; ++c) s[c] = (c < kt.valid) ? s[c] : -INFINITY;
+                for (int c = 0; c < kTile; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
             }
             // row max: four independent chains of 3-input max, then combined
             float m4[4] = {s[0], s[1], s[2], s[3]};
@@ -328,7 +339,9 @@ __global__ void __launch_bounds__(320, 1)
                     tmem_st32(to + c4 * 32, r);
                 }
             }
-            const float neg_m = -m_run;
+            // A row that has seen no key yet (causal variant) has m_run = -inf:
+            // its P is exp2(-inf) = 0 rather than exp2(-inf + inf).
+            const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};  // 8 sum chains
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // P in two halves of 64 keys (32 columns each)

@@ -236,10 +236,11 @@ size_t tt_block_attn_workspace_bytes(tt_handle h, const tt_attn_desc* d) {
     return pl.ws_bytes;
 }
 
-int tt_block_attn(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
-                  const void* v_blk, const void* k_ctx, const void* v_ctx,
-                  const int32_t* ctx_len, void* out, void* workspace, size_t workspace_bytes,
-                  void* stream) {
+// Body of tt_block_attn (causal = 0) and tt_block_attn_causal (causal = 1).
+static int block_attn_call(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
+                           const void* v_blk, const void* k_ctx, const void* v_ctx,
+                           const int32_t* ctx_len, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream, int causal) {
     if (!h) return fail(TT_ERR_INVALID_ARG, "tt_block_attn: handle is NULL");
     AttnPlan pl;
     int st = plan_attn(d, h->num_sms, &pl);
@@ -295,6 +296,7 @@ int tt_block_attn(tt_handle h, const tt_attn_desc* d, const void* q, const void*
     tt::AttnParams p;
     p.B = B; p.L = L; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.ctx_cap = d->ctx_cap;
     p.n_mtiles = pl.n_mtiles; p.n_pairs = pl.n_pairs; p.chunk = pl.chunk; p.nblk = pl.nblk;
+    p.causal = causal;
     const float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(D));
     p.scale_log2 = scale * 1.4426950408889634f;
     p.ctx_len = ctx_len;
@@ -311,6 +313,55 @@ int tt_block_attn(tt_handle h, const tt_attn_desc* d, const void* q, const void*
         e = tt::launch_attn_merge(p, D, s);
         if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
     }
+    return TT_OK;
+}
+
+int tt_block_attn(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
+                  const void* v_blk, const void* k_ctx, const void* v_ctx,
+                  const int32_t* ctx_len, void* out, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+    return block_attn_call(h, d, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out, workspace,
+                           workspace_bytes, stream, 0);
+}
+
+int tt_block_attn_causal(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
+                         const void* v_blk, const void* k_ctx, const void* v_ctx,
+                         const int32_t* ctx_len, void* out, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    return block_attn_call(h, d, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out, workspace,
+                           workspace_bytes, stream, 1);
+}
+
+int tt_kv_append(tt_handle h, const tt_attn_desc* d, const void* k_blk, const void* v_blk,
+                 void* k_ctx, void* v_ctx, int32_t* ctx_len, void* stream) {
+    if (!h) return fail(TT_ERR_INVALID_ARG, "tt_kv_append: handle is NULL");
+    if (!d) return fail(TT_ERR_INVALID_ARG, "tt_kv_append: desc is NULL");
+    if (d->B < 0 || d->B > 65535) return fail(TT_ERR_INVALID_ARG, "B=%d outside [0, 65535]", d->B);
+    if (d->D != 64 && d->D != 128)
+        return fail(TT_ERR_UNSUPPORTED, "head dim D=%d unsupported (64 or 128)", d->D);
+    if (d->Hkv < 1 || d->Hkv > 65535) return fail(TT_ERR_INVALID_ARG, "Hkv=%d outside [1, 65535]", d->Hkv);
+    if (d->ctx_cap < 1 || d->ctx_cap > (1 << 24))
+        return fail(TT_ERR_INVALID_ARG, "ctx_cap=%d outside [1, 2^24]", d->ctx_cap);
+    if (d->L < 1 || d->L > d->ctx_cap)
+        return fail(TT_ERR_INVALID_ARG, "L=%d outside [1, ctx_cap=%d]", d->L, d->ctx_cap);
+    if (d->B == 0) return TT_OK;
+    if (!k_blk || !v_blk || !k_ctx || !v_ctx || !ctx_len)
+        return fail(TT_ERR_INVALID_ARG, "tt_kv_append: a tensor pointer is NULL");
+    if (!aligned16(k_blk) || !aligned16(v_blk) || !aligned16(k_ctx) || !aligned16(v_ctx) ||
+        (reinterpret_cast<uintptr_t>(ctx_len) & 3u))
+        return fail(TT_ERR_INVALID_ARG, "tt_kv_append: tensors must be 16-byte aligned");
+    DeviceGuard g(h->device);
+    if (!g.ok()) return fail(TT_ERR_CUDA, "cannot select device %d", h->device);
+    tt::KvAppendParams p;
+    p.B = d->B; p.L = d->L; p.Hkv = d->Hkv; p.D = d->D; p.ctx_cap = d->ctx_cap;
+    p.k_blk = static_cast<const __nv_bfloat16*>(k_blk);
+    p.v_blk = static_cast<const __nv_bfloat16*>(v_blk);
+    p.k_ctx = static_cast<__nv_bfloat16*>(k_ctx);
+    p.v_ctx = static_cast<__nv_bfloat16*>(v_ctx);
+    p.ctx_len = ctx_len;
+    p.status = h->status;
+    const cudaError_t e = tt::launch_kv_append(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kv append launch");
     return TT_OK;
 }
 

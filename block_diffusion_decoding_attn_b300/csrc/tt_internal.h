@@ -20,6 +20,7 @@ struct AttnParams {
     int n_pairs;   // ceil(n_mtiles / 2): a CTA takes two query tiles
     int chunk;     // KV tiles per split
     int nblk;      // ceil(L / 128) tiles of block keys
+    int causal;    // 1: block query l sees block keys 0..l only (context-tower update)
     float scale_log2;
     const int32_t* ctx_len;
     __nv_bfloat16* out;
@@ -39,6 +40,20 @@ int attn_smem_bytes(int D);
 cudaError_t launch_block_attn(const AttnMaps& maps, const AttnParams& p, int D, int splits,
                               cudaStream_t s);
 cudaError_t launch_attn_merge(const AttnParams& p, int D, cudaStream_t s);
+
+struct KvAppendParams {
+    int B, L, Hkv, D, ctx_cap;
+    const __nv_bfloat16* k_blk;  // [B][L][Hkv][D]
+    const __nv_bfloat16* v_blk;
+    __nv_bfloat16* k_ctx;        // [B][Hkv][ctx_cap][D]
+    __nv_bfloat16* v_ctx;
+    int32_t* ctx_len;            // [B], advanced by L where the block fits
+    unsigned* status;
+};
+
+// Copies the block's K/V rows to cache positions ctx_len[b] .. ctx_len[b] + L - 1,
+// then advances ctx_len[b] by L (two launches on stream s).
+cudaError_t launch_kv_append(const KvAppendParams& p, cudaStream_t s);
 
 struct CommitParams {
     const float* logits;

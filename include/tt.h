@@ -44,7 +44,8 @@ typedef enum {
 } tt_status;
 
 /* Bits of the device status word (tt_get_error). */
-#define TT_DEV_CTX_LEN_RANGE 1u /* a ctx_len[b] outside [0, ctx_cap] (it was clamped) */
+#define TT_DEV_CTX_LEN_RANGE 1u /* a ctx_len[b] outside [0, ctx_cap] (it was clamped), or a block
+                                   that does not fit the cache (tt_kv_append skipped it) */
 #define TT_DEV_WAIT_TIMEOUT 2u  /* a bounded pipeline wait gave up; outputs invalid    */
 
 typedef struct tt_context* tt_handle;
@@ -114,6 +115,42 @@ int tt_block_attn(tt_handle handle, const tt_attn_desc* desc, const void* q, con
                   const void* v_blk, const void* k_ctx, const void* v_ctx,
                   const int32_t* ctx_len, void* out, void* workspace, size_t workspace_bytes,
                   void* stream);
+
+/* ------------------------------------------------------------------------
+ * Context-tower update after a commit -- Section 2.1, Algorithm 1, step 8
+ * ("update AR context"): once a block is clean, the context tower runs its
+ * tokens causally over the prefix cache and the block's keys/values join the
+ * cache. Per attention layer that is tt_block_attn_causal followed by
+ * tt_kv_append.
+ *
+ * tt_block_attn_causal: the same call as tt_block_attn (same arguments,
+ * layouts, arithmetic, workspace and errors) except that block query l sees
+ * the ctx_len[b] cache positions and block keys 0..l only:
+ *   out[b][l][h] = softmax over [K_ctx[0..C_b-1]; K_blk[0..l]] applied to V.
+ * With L == 1 it equals tt_block_attn (one autoregressive decode row).
+ * ------------------------------------------------------------------------ */
+int tt_block_attn_causal(tt_handle handle, const tt_attn_desc* desc, const void* q,
+                         const void* k_blk, const void* v_blk, const void* k_ctx,
+                         const void* v_ctx, const int32_t* ctx_len, void* out, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* tt_kv_append: copies the block's keys and values into the cache behind the
+ * positions already there and advances the lengths:
+ *   k_ctx[b][h][ctx_len[b] + l][:] = k_blk[b][l][h][:]   (same for v), l < L
+ *   ctx_len[b] += L
+ * for every b with 0 <= ctx_len[b] <= ctx_cap - L. A block that does not fit
+ * is skipped (cache and ctx_len[b] unchanged) and sets TT_DEV_CTX_LEN_RANGE.
+ * desc gives B, L, Hkv, D and ctx_cap (Hq, scale and num_splits are not used);
+ * layouts as for tt_block_attn: k_blk/v_blk [B][L][Hkv][D] bf16, k_ctx/v_ctx
+ * [B][Hkv][ctx_cap][D] bf16 (written), ctx_len [B] int32 (read and written),
+ * all device pointers, 16-byte aligned. Cache rows outside the appended range
+ * are not touched. Two launches on `stream` (the copy, then the lengths), no
+ * workspace. Supported: D in {64, 128}, 1 <= L <= ctx_cap, Hkv >= 1, B >= 0.
+ * Host errors: TT_ERR_INVALID_ARG for a NULL or misaligned pointer or a
+ * descriptor outside the supported range.
+ * ------------------------------------------------------------------------ */
+int tt_kv_append(tt_handle handle, const tt_attn_desc* desc, const void* k_blk, const void* v_blk,
+                 void* k_ctx, void* v_ctx, int32_t* ctx_len, void* stream);
 
 /* ------------------------------------------------------------------------
  * Unmask / commit -- Section 2.2, "Sampling", Algorithm 2 (ConfidenceSample),

@@ -13,6 +13,9 @@ method's arithmetic.
 * ``commit`` follows Section 2.2 / Algorithm 2 (confidence unmasking) with a
   fixed per-step budget k and the canonical fixed-point confidence key
   (``commit_ref.c``).
+* ``block_attn(..., causal=True)`` and ``kv_append`` follow Section 2.1,
+  Algorithm 1, "update AR context": the context tower's causal pass over a
+  committed block, and its keys/values joining the prefix cache.
 """
 from __future__ import annotations
 
@@ -51,6 +54,8 @@ def _load():
             lib.tt_oracle_block_attn.restype = ctypes.c_int
             lib.tt_oracle_block_attn.argtypes = [ctypes.c_int] * 6 + [ctypes.c_double] + [P] * 6 + [
                 ctypes.c_int, P, P, ctypes.c_int]
+            lib.tt_oracle_block_attn_causal.restype = ctypes.c_int
+            lib.tt_oracle_block_attn_causal.argtypes = lib.tt_oracle_block_attn.argtypes
             lib.tt_oracle_exp_own.restype = ctypes.c_float
             lib.tt_oracle_exp_own.argtypes = [ctypes.c_float]
             lib.tt_oracle_quant.restype = ctypes.c_uint64
@@ -78,8 +83,9 @@ def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
 
 
-def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, scale=None, rows=None, threads=0):
-    """fp64 block attention (Eq. 1).
+def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, scale=None, rows=None, threads=0,
+               causal=False):
+    """fp64 block attention (Eq. 1); ``causal``: block query l sees block keys 0..l only.
 
     q [B][L][Hq][D], k_blk/v_blk [B][L][Hkv][D], k_ctx/v_ctx [B][Hkv][C_cap][D]
     as bf16 bit patterns (uint16); ctx_len [B] int32. ``scale`` None means
@@ -103,12 +109,40 @@ def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, scale=None, rows=None, th
         rows = _c(rows, np.int32).reshape(-1, 3)
         out = np.empty((rows.shape[0], D), np.float64)
         n, rp = rows.shape[0], _ptr(rows)
-    rc = lib.tt_oracle_block_attn(B, L, Hq, Hkv, D, C, float(scale), _ptr(q), _ptr(k_blk),
-                                  _ptr(v_blk), _ptr(k_ctx), _ptr(v_ctx), _ptr(ctx_len), n, rp,
-                                  _ptr(out), int(threads))
+    fn = lib.tt_oracle_block_attn_causal if causal else lib.tt_oracle_block_attn
+    rc = fn(B, L, Hq, Hkv, D, C, float(scale), _ptr(q), _ptr(k_blk), _ptr(v_blk), _ptr(k_ctx),
+            _ptr(v_ctx), _ptr(ctx_len), n, rp, _ptr(out), int(threads))
     if rc != 0:
         raise ValueError("oracle block_attn: invalid arguments")
     return out
+
+
+def kv_append(k_blk, v_blk, k_ctx, v_ctx, ctx_len):
+    """The cache after a committed block joins it (Algorithm 1, "update AR context").
+
+    k_blk/v_blk [B][L][Hkv][D], k_ctx/v_ctx [B][Hkv][C_cap][D] (any element
+    type), ctx_len [B]. Returns new (k_ctx, v_ctx, ctx_len, fits): for every b
+    with 0 <= ctx_len[b] <= C_cap - L, cache rows ctx_len[b] + l take block row
+    l and ctx_len[b] grows by L; any other b is left as it was (fits[b] False).
+    The inputs are not modified.
+    """
+    k_blk, v_blk = np.asarray(k_blk), np.asarray(v_blk)
+    k_new, v_new = np.array(k_ctx, copy=True), np.array(v_ctx, copy=True)
+    n_new = np.array(ctx_len, dtype=np.int64, copy=True)
+    B, L, Hkv, D = k_blk.shape
+    cap = k_new.shape[2]
+    fits = np.zeros(B, dtype=bool)
+    for b in range(B):
+        c = int(n_new[b])
+        if c < 0 or c + L > cap:
+            continue
+        fits[b] = True
+        for l in range(L):
+            for h in range(Hkv):
+                k_new[b, h, c + l, :] = k_blk[b, l, h, :]
+                v_new[b, h, c + l, :] = v_blk[b, l, h, :]
+        n_new[b] = c + L
+    return k_new, v_new, n_new.astype(np.int32), fits
 
 
 def exp_own(x: float) -> float:

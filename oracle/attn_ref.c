@@ -15,6 +15,12 @@
  * Causality towards past clean blocks holds because the cache only holds past
  * positions.
  *
+ * Causal variant (tt_oracle_block_attn_causal): the context tower's pass
+ * over a committed block (Section 2.1, Algorithm 1, "update AR context": the
+ * context tower processes the committed tokens causally). Block query l
+ * takes its softmax over the cache positions and block keys 0..l only, i.e.
+ * the key list above cut after block key l.
+ *
  * Readings (the pages are silent on these): query head h uses KV head
  * floor(h / (Hq/Hkv)); the score scale is a parameter (1/sqrt(D) by default);
  * no positional encoding is applied here.
@@ -40,10 +46,11 @@ static inline double bf16_to_double(uint16_t b) {
 static void attn_row(int L, int Hq, int Hkv, int D, int ctx_cap, double scale,
                      const uint16_t* q, const uint16_t* k_blk, const uint16_t* v_blk,
                      const uint16_t* k_ctx, const uint16_t* v_ctx, int C, int b, int l,
-                     int h, double* s, double* out) {
+                     int h, int causal, double* s, double* out) {
     const int G = Hq / Hkv;
     const int kv = h / G;
-    const int N = C + L; /* concatenated key list: context, then block */
+    /* concatenated key list: context, then block (causal: block keys 0..l) */
+    const int N = C + (causal ? l + 1 : L);
     const uint16_t* qr = q + (((size_t)b * L + l) * Hq + h) * D;
 
     /* scores s_j = scale * <q, k_j> */
@@ -77,11 +84,11 @@ static void attn_row(int L, int Hq, int Hkv, int D, int ctx_cap, double scale,
  * Returns 0, or -1 on an argument error (ctx_len outside [0, ctx_cap],
  * Hq not a multiple of Hkv, a row triple out of range).
  */
-int tt_oracle_block_attn(int B, int L, int Hq, int Hkv, int D, int ctx_cap, double scale,
-                         const uint16_t* q, const uint16_t* k_blk, const uint16_t* v_blk,
-                         const uint16_t* k_ctx, const uint16_t* v_ctx,
-                         const int32_t* ctx_len, int nrows, const int32_t* rows,
-                         double* out, int nthreads) {
+static int block_attn_rows(int B, int L, int Hq, int Hkv, int D, int ctx_cap, double scale,
+                           const uint16_t* q, const uint16_t* k_blk, const uint16_t* v_blk,
+                           const uint16_t* k_ctx, const uint16_t* v_ctx,
+                           const int32_t* ctx_len, int nrows, const int32_t* rows,
+                           double* out, int nthreads, int causal) {
     if (B < 0 || L < 1 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv) return -1;
     for (int b = 0; b < B; ++b)
         if (ctx_len[b] < 0 || ctx_len[b] > ctx_cap) return -1;
@@ -110,10 +117,28 @@ int tt_oracle_block_attn(int B, int L, int Hq, int Hkv, int D, int ctx_cap, doub
                 if (rows) { b = rows[3 * i]; l = rows[3 * i + 1]; h = rows[3 * i + 2]; }
                 else { b = (int)(i / ((long)L * Hq)); l = (int)((i / Hq) % L); h = (int)(i % Hq); }
                 attn_row(L, Hq, Hkv, D, ctx_cap, scale, q, k_blk, v_blk, k_ctx, v_ctx,
-                         ctx_len[b], b, l, h, s, out + (size_t)i * D);
+                         ctx_len[b], b, l, h, causal, s, out + (size_t)i * D);
             }
             free(s);
         }
     }
     return err ? -1 : 0;
+}
+
+int tt_oracle_block_attn(int B, int L, int Hq, int Hkv, int D, int ctx_cap, double scale,
+                         const uint16_t* q, const uint16_t* k_blk, const uint16_t* v_blk,
+                         const uint16_t* k_ctx, const uint16_t* v_ctx,
+                         const int32_t* ctx_len, int nrows, const int32_t* rows,
+                         double* out, int nthreads) {
+    return block_attn_rows(B, L, Hq, Hkv, D, ctx_cap, scale, q, k_blk, v_blk, k_ctx, v_ctx,
+                           ctx_len, nrows, rows, out, nthreads, 0);
+}
+
+int tt_oracle_block_attn_causal(int B, int L, int Hq, int Hkv, int D, int ctx_cap, double scale,
+                                const uint16_t* q, const uint16_t* k_blk, const uint16_t* v_blk,
+                                const uint16_t* k_ctx, const uint16_t* v_ctx,
+                                const int32_t* ctx_len, int nrows, const int32_t* rows,
+                                double* out, int nthreads) {
+    return block_attn_rows(B, L, Hq, Hkv, D, ctx_cap, scale, q, k_blk, v_blk, k_ctx, v_ctx,
+                           ctx_len, nrows, rows, out, nthreads, 1);
 }
