@@ -216,23 +216,28 @@ __device__ __forceinline__ unsigned long long shfl_xor64(unsigned long long v, i
     return __shfl_xor_sync(0xffffffffu, v, o);
 }
 
+// One exchange message: two 64-bit words, written by st.async (16 bytes).
+struct alignas(16) XchgIn {
+    unsigned long long a, b;
+};
+constexpr uint32_t kXchgBytes = kCommitCluster * sizeof(XchgIn);  // per row and barrier
+
 struct CommitShared {
     uint64_t full[kSlots];      // producer -> pass 1: chunk landed
     uint64_t empty[kSlots];     // pass 1 -> producer: slot free (one arrival per pass-1 warp)
     uint64_t tfree[2];          // pass 2 -> pass 1: TMEM row slot free (one arrival per pass-2 warp)
     uint64_t p1_done[kXchg];    // pass 1 -> slice sender: the row's per-warp results are written
     uint64_t p2_done[kXchg];    // pass 2 -> key sender: the row's per-warp partial keys are written
-    uint64_t am_bar[kXchg];     // one arrival per CTA: its slice (max, argmax)
-    uint64_t sum_bar[kXchg];    // one arrival per CTA at CTA 0: its partial key
+    uint64_t am_bar[kXchg];     // 16 bytes from each CTA: its slice (argmax code, min)
+    uint64_t sum_bar[kXchg];    // 16 bytes from each CTA at CTA 0: (partial key, prediction)
     uint64_t col_done[kXchg];   // CTA 0: the collector has finished the row
-    unsigned long long am_in[kXchg][kCommitCluster];   // written by the cluster's CTAs
-    unsigned long long sum_in[kXchg][kCommitCluster];  // (CTA 0 only)
-    int col_arg[kXchg];                                 // (CTA 0) prediction of the row
+    XchgIn am_in[kXchg][kCommitCluster];   // (argmax code, slice min) from the cluster's CTAs
+    XchgIn sum_in[kXchg][kCommitCluster];  // (partial key, prediction) (CTA 0 only)
     int row_arg[kXchg];                                 // pass 2 -> key sender: prediction
-    float smin[2];                                      // slice minimum of each TMEM row slot
     unsigned long long red_am[kXchg][kP1Warps];
     float red_min[kXchg][kP1Warps];
     unsigned long long red_sum[kXchg][kP2Warps];
+    int xchg_err;           // a receiver gave up waiting for an exchange
     int total;              // masked rows of this cluster
     int row0;               // first row of this cluster's range
     int wsum[kThreads / 32];  // start-up scan: masked rows per warp
@@ -454,11 +459,18 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
         for (int q = 0; q < kXchg; ++q) {
             mbar_init(&sh.p1_done[q], kP1Warps);
             mbar_init(&sh.p2_done[q], kP2Warps);
-            mbar_init(&sh.am_bar[q], kCommitCluster);
-            mbar_init(&sh.sum_bar[q], kCommitCluster);
+            mbar_init(&sh.am_bar[q], 1);
+            mbar_init(&sh.sum_bar[q], 1);
             mbar_init(&sh.col_done[q], 1);
         }
         fence_mbar_init();
+        // Each exchange barrier expects the messages of its first row; the
+        // receiver re-arms it for row + kXchg once it has read a row.
+        for (int q = 0; q < kXchg; ++q) {
+            mbar_arrive_expect_tx(&sh.am_bar[q], kXchgBytes);
+            mbar_arrive_expect_tx(&sh.sum_bar[q], kXchgBytes);
+        }
+        sh.xchg_err = 0;
     }
     if (warp == 0) {
         tmem_alloc(&sh.tmem, 512);
@@ -589,14 +601,16 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 const int q = it % kXchg;
                 if (!mbar_wait_cluster(&sh.sum_bar[q], (it / kXchg) & 1, limit)) {
                     ok = false;
+                    if (lane == 0) sh.xchg_err = 1;
                     break;
                 }
                 unsigned long long key = 0;
 #pragma unroll
-                for (int j = 0; j < kCommitCluster; ++j) key += sh.sum_in[q][j];
-                const int arg = sh.col_arg[q];
+                for (int j = 0; j < kCommitCluster; ++j) key += sh.sum_in[q][j].a;
+                const int arg = static_cast<int>(sh.sum_in[q][0].b);
                 __syncwarp();
                 if (lane == 0) {
+                    mbar_arrive_expect_tx(&sh.sum_bar[q], kXchgBytes);  // for row it + kXchg
                     p.key[r] = key;
                     p.arg[r] = arg;
                     mbar_arrive(&sh.col_done[q]);
@@ -732,17 +746,25 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 const int t = seq & 1;
                 const int q = seq % kXchg;
                 ok = __all_sync(0xffffffffu, mbar_wait_cluster(&sh.am_bar[q], (seq / kXchg) & 1, limit));
-                if (!ok) break;
+                if (!ok) {
+                    if (lane == 0) sh.xchg_err = 1;
+                    break;
+                }
                 tc_fence_after();
-                unsigned long long rm = sh.am_in[q][0];
+                unsigned long long rm = sh.am_in[q][0].a;
 #pragma unroll
-                for (int k = 1; k < kCommitCluster; ++k) rm = max(rm, sh.am_in[q][k]);
+                for (int k = 1; k < kCommitCluster; ++k) rm = max(rm, sh.am_in[q][k].a);
+                const float smin = __uint_as_float(static_cast<unsigned>(sh.am_in[q][rank].b));
+                // Messages for row seq + kXchg come only after every pass-2 warp of
+                // every CTA is past this row (the rank-0 sender waits for the
+                // collector), so the barrier can be re-armed now.
+                if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&sh.am_bar[q], kXchgBytes);
                 const float m = dec_value(rm);
                 // Differences x = l - m below -31 have term 0; they are clamped
                 // there (keeps n and the exponent arithmetic in range) unless no
                 // logit of the slice needs it. Padding (-inf) clamps to a zero
                 // term, so every thread adds exactly ncol terms.
-                const bool noclamp = sh.smin[t] - m >= -31.0f;
+                const bool noclamp = smin - m >= -31.0f;
                 const f2 m2 = dup(m);
                 unsigned hi = 0, lo = 0;
                 const uint32_t tb = sh.tmem + lane_off + static_cast<uint32_t>(t * kRowCols + c0w);
@@ -782,7 +804,6 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
         } else if (warp == kAmSenderWarp) {
             // ------------------------------------------------------------ slice sender
             for (int seq = 0; seq < total && ok; ++seq) {
-                const int t = seq & 1;
                 const int q = seq % kXchg;
                 ok = __all_sync(0xffffffffu, mbar_wait(&sh.p1_done[q], (seq / kXchg) & 1, limit));
                 if (!ok) break;
@@ -798,11 +819,9 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                     ok = mbar_wait(&sh.col_done[q], ((seq / kXchg) - 1) & 1, limit);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                if (lane < kCommitCluster) {  // lane j sends to CTA j
-                    if (lane == static_cast<int>(rank)) sh.smin[t] = mnv;  // released with it
-                    st_cluster_u64(mapa_shared(smem_u32(&sh.am_in[q][rank]), lane), a);
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&sh.am_bar[q]), lane));
-                }
+                if (lane < kCommitCluster)  // lane j sends to CTA j
+                    st_async_v2_b64(mapa_shared(smem_u32(&sh.am_in[q][rank]), lane), a,
+                                    __float_as_uint(mnv), mapa_shared(smem_u32(&sh.am_bar[q]), lane));
                 __syncwarp();
             }
         } else {
@@ -814,11 +833,10 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 unsigned long long a = lane < kP2Warps ? sh.red_sum[q][lane] : 0ull;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) a += shfl_xor64(a, o);
-                if (lane == 0) {
-                    if (rank == 0) sh.col_arg[q] = sh.row_arg[q];
-                    st_cluster_u64(mapa_shared(smem_u32(&sh.sum_in[q][rank]), 0), a);
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&sh.sum_bar[q]), 0));
-                }
+                if (lane == 0)
+                    st_async_v2_b64(mapa_shared(smem_u32(&sh.sum_in[q][rank]), 0), a,
+                                    rank == 0 ? static_cast<unsigned>(sh.row_arg[q]) : 0u,
+                                    mapa_shared(smem_u32(&sh.sum_bar[q]), 0));
                 __syncwarp();
             }
         }
@@ -828,6 +846,16 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
     // No CTA leaves while another may still write into its shared memory.
     tc_fence_before();
     cluster_sync_all();
+    // A receiver that gave up may still be the target of a message issued
+    // before its sender reached the barrier above: let it land before this
+    // CTA's shared memory goes away (only after a timeout).
+    if (sh.xchg_err) {
+        if (tid == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 20000) __nanosleep(1000);
+        }
+        __syncthreads();
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(sh.tmem, 512);

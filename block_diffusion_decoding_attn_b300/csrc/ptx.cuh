@@ -127,6 +127,21 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// Stores 16 bytes (a, b) into shared memory of a CTA of the cluster and
+// signals their arrival as 16 transaction bytes on an mbarrier of that CTA
+// (complete_tx): a one-way message, with no fence or round trip at the
+// sender. The receiver arms the barrier with mbar_arrive_expect_tx for the
+// bytes of a phase; the data is visible to the threads that observe the
+// phase completing. dst must be 16-byte aligned.
+__device__ __forceinline__ void st_async_v2_b64(uint32_t cluster_dst, unsigned long long a,
+                                                unsigned long long b, uint32_t cluster_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b64 [%0], {%1, %2}, [%3];" ::"r"(
+            cluster_dst),
+        "l"(a), "l"(b), "r"(cluster_bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
