@@ -15,27 +15,26 @@
 // Layout of the work: a persistent grid of 4-CTA clusters. Cluster c owns a
 // contiguous share of the masked rows (by ordinal; the shares differ by at
 // most one row); CTA j of the cluster owns the j-th quarter of each of its
-// rows (128 KB at V = 131072). Per CTA:
-//   warp 16 (producer): for each owned masked row, bulk TMA copies of the
+// rows (128 KB at V = 131072). Per CTA (16 warps):
+//   producer (warp 12): for each owned masked row, bulk TMA copies of the
 //       CTA's quarter in 64 KB chunks into a 3-slot shared-memory ring (L2
 //       evict-first); unmasked rows are only marked in masked_out;
-//   warps 0-15 (consumers, two groups of 8 warps taking alternate rows): per
-//       row the group
-//       pass 1  streams the chunks from shared memory into its half of the
-//               tensor memory (TMEM: 128 lanes x 256 columns = one quarter row),
-//               taking the slice max / first argmax on the way and freeing each
-//               slot at once; the result goes to all 4 CTAs (DSMEM store +
-//               remote mbarrier arrive; no cluster-wide barrier)
-//       wait    for the 4 slice results   -> row max m and prediction
-//       pass 2  reads the slice back from TMEM, 32 columns at a time, and sums
-//               its fixed-point terms -> partial key sent to CTA 0;
-//       while one group waits for the cluster, the other computes, and the
-//       ring keeps streaming;
-//   warp 17 of CTA 0 (collector): adds each row's 4 partial keys, writes
+//   pass 1 (warps 0-3, one per TMEM lane quarter): streams each row's chunks
+//       from shared memory into one of two TMEM row slots (128 lanes x 256
+//       columns = one quarter row), keeping the slice max / first argmax /
+//       min, and frees each ring slot at once;
+//   slice sender (warp 14): sends the CTA's slice result to all 4 CTAs as a
+//       one-way st.async message on their exchange mbarrier;
+//   pass 2 (warps 4-11): once the 4 slice results of the row are in (row max
+//       m, prediction), reads the slot back 32 columns at a time and sums the
+//       fixed-point terms, then frees the slot;
+//   key sender (warp 15): sends the CTA's partial key to CTA 0 the same way;
+//   collector (warp 13 of CTA 0): adds each row's 4 partial keys, writes
 //       key/arg; per block it takes one ticket for all of the cluster's rows
 //       of the block (the count is the block's number of masked rows); the
 //       warp that completes the count ranks the block's masked rows and
 //       commits.
+// Pass 1 and the exchange of row i + 1 run while pass 2 works on row i.
 
 // e(x) is an fp32 exponential defined for this purpose (Cody and Waite range
 // reduction, then the degree-7 Taylor polynomial of exp, all with
@@ -78,13 +77,13 @@ constexpr int kSlots = 3;                 // ring depth: 64 KB chunks landing pe
 constexpr int kChunk = 16384;             // logits per ring slot
 constexpr int kSliceMax = 2 * kChunk;               // 32768 logits per CTA
 constexpr int kRowCols = kSliceMax / 128;           // 256 TMEM columns per row slot, 2 slots
-constexpr int kP1Warps = 8;               // pass 1: warps 0-7 (two per TMEM lane quarter)
-constexpr int kP2Warps = 8;               // pass 2: warps 8-15
+constexpr int kP1Warps = 4;               // pass 1: warps 0-3 (one per TMEM lane quarter)
+constexpr int kP2Warps = 8;               // pass 2: warps 4-11
 constexpr int kP1Threads = kP1Warps * 32;
-constexpr int kProducerWarp = kP1Warps + kP2Warps;  // warp 16
-constexpr int kCollectorWarp = kProducerWarp + 1;   // warp 17 (CTA 0 only)
-constexpr int kAmSenderWarp = kCollectorWarp + 1;   // warp 18: slice results -> the cluster
-constexpr int kSumSenderWarp = kAmSenderWarp + 1;   // warp 19: partial keys -> CTA 0
+constexpr int kProducerWarp = kP1Warps + kP2Warps;  // warp 12
+constexpr int kCollectorWarp = kProducerWarp + 1;   // warp 13 (CTA 0 only)
+constexpr int kAmSenderWarp = kCollectorWarp + 1;   // warp 14: slice results -> the cluster
+constexpr int kSumSenderWarp = kAmSenderWarp + 1;   // warp 15: partial keys -> CTA 0
 constexpr int kP1PerChunk = kChunk / kP1Threads;    // logits per pass-1 thread per chunk
 constexpr int kP2Cols = kRowCols / (kP2Warps / 4);  // TMEM columns per pass-2 thread
 constexpr int kThreads = (kSumSenderWarp + 1) * 32;
@@ -632,11 +631,11 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
     } else {
         // ---------------------------------------------------------------- pass 1 / pass 2
         // Rows of the cluster's sequence alternate between the two TMEM row
-        // slots (256 columns each). Pass 1 (warps 0-7) drains a row's chunks
+        // slots (256 columns each). Pass 1 (warps 0-3) drains a row's chunks
         // from the ring into its slot, taking the slice max / first argmax /
-        // min; warp 18 sends the result to the cluster. Pass 2 (warps 8-15)
+        // min; warp 14 sends the result to the cluster. Pass 2 (warps 4-11)
         // waits for the cluster's results of that row, sums its fixed-point
-        // terms from TMEM and frees the slot; warp 19 sends the partial key to
+        // terms from TMEM and frees the slot; warp 15 sends the partial key to
         // CTA 0. So pass 1 of row i + 1 and the exchange run while pass 2
         // works on row i, and no computing warp waits for a DSMEM send. The
         // per-warp results of row i go through slot i % kXchg of shared
