@@ -57,6 +57,16 @@ def causal_flops(w, ctx):
     return 4.0 * w.Hq * w.D * pairs
 
 
+TRAIN_B, TRAIN_N, TRAIN_S = 2, 4096, 16  # training leg: sequences, tokens, block size
+
+
+def train_flops(w, B, N, S):
+    """QK^T + PV of the batched training pass: block j's S queries see j*S clean
+    and S noisy keys."""
+    nb = N // S
+    return 4.0 * w.Hq * w.D * B * S * S * nb * (nb + 1) / 2.0
+
+
 def append_bytes(w):
     """The block's K and V read once more and written into the cache."""
     return 2.0 * (2 * 2 * w.B * w.L * w.Hkv * w.D)
@@ -501,6 +511,29 @@ def run_gpu(args, w):
     u_ms = max_over_ranks(statistics.mean(t_upd) / ncalls, dist)  # per call
     del big
 
+    # Training-time batched block attention (all noisy blocks of a clean
+    # sequence in one call), the workload's heads, TRAIN_B x TRAIN_N tokens.
+    wt = wl.custom("train", TRAIN_B, TRAIN_N, w.Hq, w.Hkv, w.D, TRAIN_N, (TRAIN_N,) * TRAIN_B)
+    Tt = wl.attn_tensors(wl.attn_inputs(wt, seed=rank), dev)
+    out_t = torch.empty_like(Tt["q"])
+
+    def train_attn():
+        tt.block_attn_train(Tt["q"], Tt["k_blk"], Tt["v_blk"], Tt["k_ctx"], Tt["v_ctx"], TRAIN_S,
+                            out=out_t, h=h, stream=stream)
+
+    evt = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ku + 2)]
+    for i in range(Ku + 2):  # the first two warm up
+        flush_l2()
+        evt[i][0].record(stream)
+        train_attn()
+        evt[i][1].record(stream)
+    torch.cuda.synchronize()
+    if h.get_error():
+        raise RuntimeError("device status set during the training-attention leg")
+    tr_ms = max_over_ranks(statistics.mean(evt[i][0].elapsed_time(evt[i][1])
+                                           for i in range(2, Ku + 2)), dist)
+    del Tt
+
     if rank != 0:
         dist.destroy_process_group() if dist else None
         return 0
@@ -535,6 +568,16 @@ def run_gpu(args, w):
                 "algorithmic": f"{fl_u:.4g} FLOP (unmasked pairs), {by_u:.4g} B {per}",
                 "ms": u_ms, "block_tokens_per_s": w.B * w.L / (u_ms * 1e-3),
                 "peak_source": peaks["source"] + " burst"}
+    fl_t = train_flops(w, TRAIN_B, TRAIN_N, TRAIN_S)
+    tr_tf = fl_t / (tr_ms * 1e-3) / 1e12
+    roof_train = {"bound": "tensor", "achieved": tr_tf, "peak": peaks["bf16_tflops"],
+                  "unit": "TFLOP/s", "frac": tr_tf / peaks["bf16_tflops"], "traffic": None,
+                  "kernel": "tt_block_attn_train: all noisy blocks of a sequence in one call "
+                            f"(B={TRAIN_B}, N={TRAIN_N}, S={TRAIN_S}, the workload's heads); "
+                            "outside the step",
+                  "algorithmic": f"{fl_t:.4g} FLOP (visible pairs) per call",
+                  "ms": tr_ms, "tokens_per_s": TRAIN_B * TRAIN_N / (tr_ms * 1e-3),
+                  "peak_source": peaks["source"] + " burst"}
     dom = roof_attn if a_ms >= c_ms else roof_comm
     line = {
         "metric": "denoised block-tokens/s per layer-step", "value": value,
@@ -544,7 +587,8 @@ def run_gpu(args, w):
         "data": "synthetic (seeded Philox normals; inputs resident in HBM)",
         "config": config_of(w, inps),
         "roofline": dom,
-        "kernels": {"attention": roof_attn, "commit": roof_comm, "context_update": roof_upd},
+        "kernels": {"attention": roof_attn, "commit": roof_comm, "context_update": roof_upd,
+                    "train_attention": roof_train},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "block-tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": Ke},

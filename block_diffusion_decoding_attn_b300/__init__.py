@@ -15,6 +15,8 @@ Entry points mirror the C ABI:
   block per step)
 * :func:`commit_threshold` -> ``tt_commit_threshold`` (Algorithm 2 with a
   confidence threshold gamma and a floor of ceil(#masked / steps_left))
+* :func:`block_attn_train` -> ``tt_block_attn_train`` (Section 2.3: all noisy
+  blocks of a clean sequence in one pass)
 * :func:`block_attn` with ``causal=True`` -> ``tt_block_attn_causal`` and
   :func:`kv_append` -> ``tt_kv_append``: the context tower's update after a
   commit (Section 2.1, Algorithm 1, "update AR context")
@@ -68,6 +70,9 @@ def lib() -> ctypes.CDLL:
             L.tt_block_attn.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 7 + [P, S, P]
             L.tt_block_attn_causal.argtypes = L.tt_block_attn.argtypes
             L.tt_kv_append.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 5 + [P]
+            L.tt_block_attn_train_workspace_bytes.restype = S
+            L.tt_block_attn_train_workspace_bytes.argtypes = [P, ctypes.POINTER(TrainDesc)]
+            L.tt_block_attn_train.argtypes = [P, ctypes.POINTER(TrainDesc)] + [P] * 6 + [P, S, P]
             L.tt_commit_workspace_bytes.restype = S
             L.tt_commit_workspace_bytes.argtypes = [I, I]
             L.tt_commit.argtypes = [P, P, I, I, I, P, I, P, P, P, S, P]
@@ -82,6 +87,12 @@ def lib() -> ctypes.CDLL:
 class AttnDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("Hq", ctypes.c_int),
                 ("Hkv", ctypes.c_int), ("D", ctypes.c_int), ("ctx_cap", ctypes.c_int),
+                ("scale", ctypes.c_float), ("num_splits", ctypes.c_int)]
+
+
+class TrainDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("S", ctypes.c_int),
+                ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
                 ("scale", ctypes.c_float), ("num_splits", ctypes.c_int)]
 
 
@@ -194,6 +205,43 @@ def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out=None, scale: float = 
     _check(fn(h.ptr, ctypes.byref(desc), _dev_ptr(q), _dev_ptr(k_blk), _dev_ptr(v_blk),
               _dev_ptr(k_ctx), _dev_ptr(v_ctx), _dev_ptr(ctx_len), _dev_ptr(out), wsp, wsn,
               _stream_ptr(q, stream)), "tt_block_attn_causal" if causal else "tt_block_attn")
+    return out
+
+
+def block_attn_train(q, k_noisy, v_noisy, k_clean, v_clean, S: int, out=None,
+                     scale: float = 0.0, num_splits: int = 0, workspace=None,
+                     h: Handle | None = None, stream=None):
+    """Training-time batched block attention (Section 2.3): noisy block j of each
+    sequence attends to the clean keys of positions 0..j*S-1 and to its own S
+    noisy keys.
+
+    q [B][N][Hq][D], k_noisy/v_noisy [B][N][Hkv][D], k_clean/v_clean [B][Hkv][N][D]
+    (torch.bfloat16, CUDA, contiguous), N a multiple of S. Returns out
+    [B][N][Hq][D] bf16.
+    """
+    import torch
+    for name, t in (("q", q), ("k_noisy", k_noisy), ("v_noisy", v_noisy), ("k_clean", k_clean),
+                    ("v_clean", v_clean)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    B, N, Hq, D = q.shape
+    Hkv = k_noisy.shape[2]
+    if tuple(k_noisy.shape) != (B, N, Hkv, D) or tuple(v_noisy.shape) != (B, N, Hkv, D) or \
+            tuple(k_clean.shape) != (B, Hkv, N, D) or tuple(v_clean.shape) != (B, Hkv, N, D):
+        raise ValueError("block_attn_train: inconsistent shapes")
+    h = h or handle(q.device.index)
+    desc = TrainDesc(B, N, int(S), Hq, Hkv, D, float(scale), int(num_splits))
+    if out is None:
+        out = torch.empty_like(q)
+    need = int(lib().tt_block_attn_train_workspace_bytes(h.ptr, ctypes.byref(desc)))
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wsp = _dev_ptr(workspace) if need else ctypes.c_void_p(0)
+    wsn = workspace.numel() * workspace.element_size() if need else 0
+    _check(lib().tt_block_attn_train(h.ptr, ctypes.byref(desc), _dev_ptr(q), _dev_ptr(k_noisy),
+                                     _dev_ptr(v_noisy), _dev_ptr(k_clean), _dev_ptr(v_clean),
+                                     _dev_ptr(out), wsp, wsn, _stream_ptr(q, stream)),
+           "tt_block_attn_train")
     return out
 
 

@@ -9,6 +9,13 @@
 // a row with no visible key in a split (a block tile past it) keeps m = -inf,
 // a zero sum and zero P there, and the merge gives such a split weight 0.
 //
+// The batched training layout (p.ctx_group = n, Section 2.3, "Implementation":
+// all noisy blocks of a clean sequence in one pass, each attending to the past
+// clean blocks and bidirectionally within itself) is the same computation
+// over B*n sequences of L = S tokens: sequence b is noisy block b % n of clean
+// sequence b / n, reads that sequence's cache and sees its first (b % n) * S
+// positions.
+//
 // One CTA owns one work unit: (sequence b, KV head, pair of 128-row query
 // tiles, KV split). The G = Hq/Hkv query heads of a KV head are packed with the
 // block positions into the M dimension (row = l*G + g), so each K/V tile staged
@@ -81,11 +88,12 @@ __global__ void __launch_bounds__(320, 1)
     const int split = blockIdx.x / p.n_pairs;
     const int kvh = blockIdx.y, b = blockIdx.z;
 
-    int C = p.ctx_len[b];
+    int C = p.ctx_group ? (b % p.ctx_group) * p.L : p.ctx_len[b];
     if (C < 0 || C > p.ctx_cap) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) atomicOr(p.status, kDevCtxLenRange);
         C = C < 0 ? 0 : p.ctx_cap;
     }
+    const int cache_b = p.ctx_group ? b / p.ctx_group : b;  // which cache sequence b reads
     const int nc = (C + kTile - 1) / kTile;
     const int nt = nc + p.nblk;
     const int t0 = split * p.chunk;
@@ -159,7 +167,7 @@ __global__ void __launch_bounds__(320, 1)
                 for (int c = 0; c < D / 64; ++c) {
                     if (t.is_ctx)
                         tma_load_3d(dst + c * Lay::kAtomBytes, is_v ? &tm_vc : &tm_kc, &full[slot],
-                                    c * 64, t.base, b * p.Hkv + kvh);
+                                    c * 64, t.base, cache_b * p.Hkv + kvh);
                     else
                         tma_load_4d(dst + c * Lay::kAtomBytes, is_v ? &tm_vb : &tm_kb, &full[slot],
                                     c * 64, kvh, t.base, b);
@@ -430,7 +438,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     const int kvh = bk % p.Hkv, b = bk / p.Hkv;
     int ns = 0;
     if (valid) {
-        int C = p.ctx_len[b];
+        int C = p.ctx_group ? (b % p.ctx_group) * p.L : p.ctx_len[b];
         C = C < 0 ? 0 : (C > p.ctx_cap ? p.ctx_cap : C);
         const int nt = (C + kTile - 1) / kTile + p.nblk;
         ns = (nt + p.chunk - 1) / p.chunk;

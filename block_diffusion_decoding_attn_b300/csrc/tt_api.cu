@@ -236,17 +236,20 @@ size_t tt_block_attn_workspace_bytes(tt_handle h, const tt_attn_desc* d) {
     return pl.ws_bytes;
 }
 
-// Body of tt_block_attn (causal = 0) and tt_block_attn_causal (causal = 1).
+// Body of tt_block_attn (causal = 0), tt_block_attn_causal (causal = 1) and
+// tt_block_attn_train (ctx_group = blocks per clean sequence: d->B counts the
+// noisy blocks, the caches belong to d->B / ctx_group clean sequences and
+// ctx_len is implied).
 static int block_attn_call(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
                            const void* v_blk, const void* k_ctx, const void* v_ctx,
                            const int32_t* ctx_len, void* out, void* workspace,
-                           size_t workspace_bytes, void* stream, int causal) {
+                           size_t workspace_bytes, void* stream, int causal, int ctx_group = 0) {
     if (!h) return fail(TT_ERR_INVALID_ARG, "tt_block_attn: handle is NULL");
     AttnPlan pl;
     int st = plan_attn(d, h->num_sms, &pl);
     if (st != TT_OK) return st;
     if (d->B == 0) return TT_OK;
-    if (!q || !k_blk || !v_blk || !ctx_len || !out)
+    if (!q || !k_blk || !v_blk || (!ctx_len && !ctx_group) || !out)
         return fail(TT_ERR_INVALID_ARG, "tt_block_attn: a tensor pointer is NULL");
     if (d->ctx_cap > 0 && (!k_ctx || !v_ctx))
         return fail(TT_ERR_INVALID_ARG, "tt_block_attn: k_ctx/v_ctx NULL with ctx_cap > 0");
@@ -285,7 +288,7 @@ static int block_attn_call(tt_handle h, const tt_attn_desc* d, const void* q, co
         // only need to be well formed, so they point at the block keys.
         const bool none = d->ctx_cap == 0;
         const cuuint64_t dims[3] = {(cuuint64_t)D, none ? (cuuint64_t)tt::kTile : (cuuint64_t)d->ctx_cap,
-                                    none ? 1 : (cuuint64_t)B * Hkv};
+                                    none ? 1 : (cuuint64_t)(ctx_group ? B / ctx_group : B) * Hkv};
         const cuuint64_t str[2] = {D * e2, (none ? (cuuint64_t)tt::kTile : (cuuint64_t)d->ctx_cap) * D * e2};
         const cuuint32_t box[3] = {64, (cuuint32_t)tt::kTile, 1};
         void* kc = none ? const_cast<void*>(k_blk) : const_cast<void*>(k_ctx);
@@ -297,6 +300,7 @@ static int block_attn_call(tt_handle h, const tt_attn_desc* d, const void* q, co
     p.B = B; p.L = L; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.ctx_cap = d->ctx_cap;
     p.n_mtiles = pl.n_mtiles; p.n_pairs = pl.n_pairs; p.chunk = pl.chunk; p.nblk = pl.nblk;
     p.causal = causal;
+    p.ctx_group = ctx_group;
     const float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(D));
     p.scale_log2 = scale * 1.4426950408889634f;
     p.ctx_len = ctx_len;
@@ -330,6 +334,47 @@ int tt_block_attn_causal(tt_handle h, const tt_attn_desc* d, const void* q, cons
                          size_t workspace_bytes, void* stream) {
     return block_attn_call(h, d, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out, workspace,
                            workspace_bytes, stream, 1);
+}
+
+// Checks a training-layout descriptor and gives the equivalent per-block one.
+static int train_desc(const tt_train_desc* t, tt_attn_desc* d) {
+    if (!t) return fail(TT_ERR_INVALID_ARG, "tt_block_attn_train: desc is NULL");
+    if (t->B < 0) return fail(TT_ERR_INVALID_ARG, "B=%d < 0", t->B);
+    if (t->S < 1 || t->N < t->S || t->N % t->S)
+        return fail(TT_ERR_INVALID_ARG, "N=%d must be a positive multiple of the block size S=%d",
+                    t->N, t->S);
+    const long blocks = static_cast<long>(t->B) * (t->N / t->S);
+    if (blocks > 65535)
+        return fail(TT_ERR_UNSUPPORTED, "B * N / S = %ld noisy blocks (at most 65535)", blocks);
+    d->B = static_cast<int>(blocks);
+    d->L = t->S;
+    d->Hq = t->Hq;
+    d->Hkv = t->Hkv;
+    d->D = t->D;
+    d->ctx_cap = t->N;
+    d->scale = t->scale;
+    d->num_splits = t->num_splits;
+    return TT_OK;
+}
+
+size_t tt_block_attn_train_workspace_bytes(tt_handle h, const tt_train_desc* t) {
+    tt_attn_desc d;
+    if (!h || train_desc(t, &d) != TT_OK) return 0;
+    AttnPlan pl;
+    if (plan_attn(&d, h->num_sms, &pl) != TT_OK) return 0;
+    return pl.ws_bytes;
+}
+
+int tt_block_attn_train(tt_handle h, const tt_train_desc* t, const void* q, const void* k_noisy,
+                        const void* v_noisy, const void* k_clean, const void* v_clean, void* out,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (!h) return fail(TT_ERR_INVALID_ARG, "tt_block_attn_train: handle is NULL");
+    tt_attn_desc d;
+    const int st = train_desc(t, &d);
+    if (st != TT_OK) return st;
+    if (t->B == 0) return TT_OK;
+    return block_attn_call(h, &d, q, k_noisy, v_noisy, k_clean, v_clean, nullptr, out, workspace,
+                           workspace_bytes, stream, 0, t->N / t->S);
 }
 
 int tt_kv_append(tt_handle h, const tt_attn_desc* d, const void* k_blk, const void* v_blk,

@@ -21,6 +21,10 @@ struct AttnParams {
     int chunk;     // KV tiles per split
     int nblk;      // ceil(L / 128) tiles of block keys
     int causal;    // 1: block query l sees block keys 0..l only (context-tower update)
+    // Batched training layout (0: off). Sequence b is noisy block b % ctx_group
+    // of clean sequence b / ctx_group: it reads that sequence's cache, with
+    // ctx_len = (b % ctx_group) * L (ctx_len is then not read).
+    int ctx_group;
     float scale_log2;
     const int32_t* ctx_len;
     __nv_bfloat16* out;

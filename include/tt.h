@@ -153,6 +153,41 @@ int tt_kv_append(tt_handle handle, const tt_attn_desc* desc, const void* k_blk, 
                  void* k_ctx, void* v_ctx, int32_t* ctx_len, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Training-time batched block attention -- Section 2.3, "Implementation":
+ * the denoiser processes all noisy blocks of a clean sequence in one forward
+ * pass; its attention attends to the past clean blocks (the frozen context
+ * tower's keys/values of the clean sequence) and bidirectionally within the
+ * current noisy block. For a sequence of N = n*S tokens, noisy block j
+ * (tokens j*S .. j*S+S-1) takes, per query, one softmax over
+ *   [K_clean[0 .. j*S-1] ; K_noisy[j*S .. j*S+S-1]]   (block 0: its own keys only)
+ * applied to the matching values. This is tt_block_attn over the B*n noisy
+ * blocks with ctx_len = j*S, every block of a sequence reading that
+ * sequence's clean cache; arithmetic, tolerance and errors as there.
+ *
+ * Layouts (bf16, row-major, contiguous, 16-byte aligned, device):
+ *   q        [B][N][Hq][D]    queries of the noisy tokens
+ *   k_noisy  [B][N][Hkv][D]   keys/values of the noisy tokens (denoiser)
+ *   v_noisy  [B][N][Hkv][D]
+ *   k_clean  [B][Hkv][N][D]   keys/values of the clean tokens (context tower)
+ *   v_clean  [B][Hkv][N][D]     only positions below the block's start are read
+ *   out      [B][N][Hq][D]
+ * Supported: as tt_block_attn with L = S; N a multiple of S; B*N/S <= 65535.
+ * Workspace: tt_block_attn_train_workspace_bytes (0 when no KV split is used).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int B, N, S, Hq, Hkv, D;
+    float scale;    /* softmax scale; 0 selects 1/sqrt(D) */
+    int num_splits; /* KV splits per (block, kv head, query tile); 0 = automatic */
+} tt_train_desc;
+
+size_t tt_block_attn_train_workspace_bytes(tt_handle handle, const tt_train_desc* desc);
+
+int tt_block_attn_train(tt_handle handle, const tt_train_desc* desc, const void* q,
+                        const void* k_noisy, const void* v_noisy, const void* k_clean,
+                        const void* v_clean, void* out, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* ------------------------------------------------------------------------
  * Unmask / commit -- Section 2.2, "Sampling", Algorithm 2 (ConfidenceSample),
  * read as a fixed budget of k commits per block per step (the threshold rule
  * with gamma > 1 and T = L/k steps).

@@ -13,6 +13,10 @@ method's arithmetic.
 * ``commit`` follows Section 2.2 / Algorithm 2 (confidence unmasking) with a
   fixed per-step budget k and the canonical fixed-point confidence key
   (``commit_ref.c``).
+* ``block_attn_train`` follows Section 2.3, "Implementation": all noisy blocks
+  of a clean sequence in one pass, block j attending to the clean positions
+  before it and bidirectionally to itself (a loop over blocks of
+  ``block_attn``).
 * ``block_attn(..., causal=True)`` and ``kv_append`` follow Section 2.1,
   Algorithm 1, "update AR context": the context tower's causal pass over a
   committed block, and its keys/values joining the prefix cache.
@@ -114,6 +118,38 @@ def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, scale=None, rows=None, th
             _ptr(v_ctx), _ptr(ctx_len), n, rp, _ptr(out), int(threads))
     if rc != 0:
         raise ValueError("oracle block_attn: invalid arguments")
+    return out
+
+
+def block_attn_train(q, k_noisy, v_noisy, k_clean, v_clean, S, scale=None, rows=None, threads=0):
+    """Training-time batched block attention (Section 2.3, "Implementation").
+
+    q [B][N][Hq][D], k_noisy/v_noisy [B][N][Hkv][D], k_clean/v_clean [B][Hkv][N][D]
+    (bf16 bit patterns). Noisy block j (tokens j*S .. j*S+S-1) of every sequence
+    attends to [clean positions 0..j*S-1 ; its own S noisy tokens]: Eq. (1)
+    with the clean sequence as the context cache and ctx_len = j*S. ``rows``
+    None gives [B][N][Hq][D]; otherwise (b, n, h) triples and an [n][D] output.
+    """
+    q = _c(q, np.uint16)
+    B, N, Hq, D = q.shape
+    if S < 1 or N % S:
+        raise ValueError("oracle block_attn_train: N must be a multiple of S")
+    if rows is None:
+        out = np.empty((B, N, Hq, D), np.float64)
+        for j in range(N // S):
+            sl = slice(j * S, (j + 1) * S)
+            out[:, sl] = block_attn(q[:, sl], k_noisy[:, sl], v_noisy[:, sl], k_clean, v_clean,
+                                    np.full(B, j * S, np.int32), scale=scale, threads=threads)
+        return out
+    rows = _c(rows, np.int32).reshape(-1, 3)
+    out = np.empty((rows.shape[0], D), np.float64)
+    for j in np.unique(rows[:, 1] // S):
+        sel = np.nonzero(rows[:, 1] // S == j)[0]
+        sub = rows[sel].copy()
+        sub[:, 1] -= j * S
+        sl = slice(j * S, (j + 1) * S)
+        out[sel] = block_attn(q[:, sl], k_noisy[:, sl], v_noisy[:, sl], k_clean, v_clean,
+                              np.full(B, j * S, np.int32), scale=scale, rows=sub, threads=threads)
     return out
 
 
