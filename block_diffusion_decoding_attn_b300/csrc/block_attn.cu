@@ -174,13 +174,15 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 issued = li + 1;
             }
-            if (!ok) {
-                atomicOr(p.status, kDevWaitTimeout);
-                // Let the copies already issued land before the CTA can exit.
-                mbar_wait(q_full, 0, limit);
-                for (int li = issued - kRing < 0 ? 0 : issued - kRing; li < issued; ++li)
-                    mbar_wait(&full[li % kRing], (li / kRing) & 1, limit);
-            }
+            if (!ok) atomicOr(p.status, kDevWaitTimeout);
+            // Let the copies already issued land before the CTA can exit (a load
+            // is issued only once the load kRing before it was consumed, so at
+            // most the last kRing can be in flight; after a normal run they
+            // have all landed). Also after a timeout of another role.
+            const uint64_t dl = drain_limit(limit);
+            mbar_wait(q_full, 0, dl);
+            for (int li = issued - kRing < 0 ? 0 : issued - kRing; li < issued; ++li)
+                mbar_wait(&full[li % kRing], (li / kRing) & 1, dl);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(320, 1)
         // No MMA may still be running when the TMEM is released.
         if (lane == 0) tc_commit(drain);
         __syncwarp();
-        mbar_wait(drain, 0, limit);
+        mbar_wait(drain, 0, drain_limit(limit));
     } else {
         // ------------------------------------------------------------ softmax
         const int x = warp >> 2;               // query tile

@@ -561,12 +561,14 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                     }
                 }
             }
-            if (!ok) {
-                atomicOr(p.status, kDevWaitTimeout);
-                // Let the copies already issued land before the CTA can exit.
-                for (int j = it - kSlots < 0 ? 0 : it - kSlots; j < it; ++j)
-                    mbar_wait(&sh.full[j % kSlots], (j / kSlots) & 1, limit);
-            }
+            if (!ok) atomicOr(p.status, kDevWaitTimeout);
+            // Let the copies already issued land before the CTA can exit (an
+            // entry is issued only once the one kSlots before it was consumed, so
+            // at most the last kSlots can be in flight; after a normal run they
+            // have all landed). Also when a consumer gave up instead.
+            const uint64_t dl = drain_limit(limit);
+            for (int j = it - kSlots < 0 ? 0 : it - kSlots; j < it; ++j)
+                mbar_wait(&sh.full[j % kSlots], (j / kSlots) & 1, dl);
         }
         __syncwarp();
     } else if (warp == kCollectorWarp) {
@@ -846,12 +848,12 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
     tc_fence_before();
     cluster_sync_all();
     // A receiver that gave up may still be the target of a message issued
-    // before its sender reached the barrier above: let it land before this
-    // CTA's shared memory goes away (only after a timeout).
+    // before its sender reached the barrier above: give it 100 us to land
+    // before this CTA's shared memory goes away (only after a timeout).
     if (sh.xchg_err) {
         if (tid == 0) {
             const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < 20000) __nanosleep(1000);
+            while (globaltimer_ns() - t0 < 100000) __nanosleep(1000);
         }
         __syncthreads();
     }

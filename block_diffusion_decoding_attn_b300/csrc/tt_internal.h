@@ -11,6 +11,13 @@ namespace tt {
 // Device status bits (accumulated in the handle's status word).
 constexpr unsigned kDevCtxLenRange = 1u;  // ctx_len[b] outside [0, ctx_cap]; clamped
 constexpr unsigned kDevWaitTimeout = 2u;  // a bounded pipeline wait gave up
+// Bound of the waits for work a CTA issued itself (its TMA copies, its MMAs)
+// before it leaves, whatever the pipeline wait limit: that work always
+// completes, and the CTA's shared and tensor memory must outlive it.
+constexpr unsigned long long kDrainNs = 100000000ull;  // 100 ms
+__host__ __device__ inline unsigned long long drain_limit(unsigned long long limit) {
+    return limit > kDrainNs ? limit : kDrainNs;
+}
 
 constexpr int kTile = 128;  // query rows per M tile and keys per KV tile
 
