@@ -44,6 +44,14 @@ def test_host_argument_errors(tt):
     assert lib.tt_block_attn(None, ctypes.byref(d), *([None] * 7), None, 0, None) == -1
     assert lib.tt_block_attn_workspace_bytes(None, ctypes.byref(d)) == 0
     assert lib.tt_create(None, 0) == -1
+    # the context-tower update and the training layout check the handle first too
+    assert lib.tt_block_attn_causal(None, ctypes.byref(d), *([None] * 7), None, 0, None) == -1
+    assert lib.tt_kv_append(None, ctypes.byref(d), *([None] * 5), None) == -1
+    assert b"tt_kv_append" in lib.tt_last_error()
+    t = tt.TrainDesc(1, 64, 16, 4, 1, 64, 0.0, 0)
+    assert lib.tt_block_attn_train(None, ctypes.byref(t), *([None] * 6), None, 0, None) == -1
+    assert b"tt_block_attn_train" in lib.tt_last_error()
+    assert lib.tt_block_attn_train_workspace_bytes(None, ctypes.byref(t)) == 0
 
 
 def test_create_without_gpu_fails_cleanly(tt):
