@@ -71,6 +71,8 @@ def test_tiny_full_denoise_loop(tt, oracle_lib):
     (2, 24, 512, 100, 0.5),     # k above #masked: commit all
     (1, 1, 4, 1, 1.0),          # smallest shape
     (2, 1030, 256, 9, 0.8),     # L above the select kernel's 1024 threads
+    (2, 24, 100000, 5, 0.8),    # each CTA's quarter ends in a partial 16384-logit chunk
+    (1, 16, 131068, 3, 1.0),    # largest V below the limit: the last quarter is ragged
 ])
 def test_shapes_and_masks(tt, oracle_lib, case):
     B, L, V, k, frac = case
@@ -79,6 +81,27 @@ def test_shapes_and_masks(tt, oracle_lib, case):
     masked = wl.random_mask(w, frac, seed=5) if frac < 1 else np.ones(w.rows, np.uint8)
     tok = np.arange(w.rows, dtype=np.int32) + 7
     _check_step(tt, oracle_lib, lg, B, L, masked, k, tok)
+
+
+def test_argmax_in_partial_chunks_and_every_quarter(tt, oracle_lib):
+    # V = 100000: quarters of 25000 logits, the second chunk of each holds
+    # 8616. Plant each row's maximum in a different place: the last logit of
+    # a quarter (inside its partial chunk), the first logit of a quarter, a
+    # tie between two quarters (the lower id wins), and the last logit of the row.
+    V = 100000
+    w = wl.custom("plant", 2, 16, 1, 1, 8, 8, (0, 0), V=V, k=4)
+    lg = wl.logits(w, seed=13)
+    spots = [24999, 25000, 49999, 50000, 74999, 75000, 99999, 16383, 16384, 41383, 41384,
+             0, 66383, 91384, 12345, 99996]
+    for r, v in enumerate(spots):
+        lg[r, v] = 30.0
+    lg[16, [30000, 80000]] = 30.0    # tie across quarters -> 30000
+    lg[17, [24999, 25000]] = 30.0    # tie across the quarter boundary -> 24999
+    lg[18, :] = -2.0
+    lg[18, 99999] = -1.0             # the maximum is the very last logit
+    masked = np.ones(w.rows, np.uint8)
+    tok = np.full(w.rows, -1, np.int32)
+    _check_step(tt, oracle_lib, lg, 2, 16, masked, 4, tok)
 
 
 def test_ties_and_alias(tt, oracle_lib):
