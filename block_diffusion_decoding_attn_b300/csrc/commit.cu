@@ -50,6 +50,8 @@
 // exponent field, and rint splits into a multiple of 2^20 plus a remainder,
 // both read out of the bits of exact fp32 sums. The arithmetic runs on packed
 // f32x2 pairs (each half rounded exactly like the scalar operation).
+#include <atomic>
+
 #include "ptx.cuh"
 #include "tt_internal.h"
 
@@ -871,10 +873,12 @@ size_t commit_smem_bytes(int /*V*/, int /*L*/) {
 }
 
 int commit_max_clusters() {
-    static int cached[64] = {};
+    // per device, filled on first use; handles on several host threads may ask at once
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-    if (cached[dev] > 0) return cached[dev];
+    const int known = cached[dev].load(std::memory_order_relaxed);
+    if (known > 0) return known;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kCommitCluster * 256, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -886,7 +890,7 @@ int commit_max_clusters() {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         n = sms / kCommitCluster > 0 ? sms / kCommitCluster : 1;
     }
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
