@@ -19,7 +19,7 @@ Entry points mirror the C ABI:
   blocks of a clean sequence in one pass)
 * :func:`block_attn` with ``causal=True`` -> ``tt_block_attn_causal`` and
   :func:`kv_append` -> ``tt_kv_append``: the context tower's update after a
-  commit (Section 2.1, Algorithm 1, "update AR context")
+  commit (Section 2.1, Algorithm 1)
 """
 from __future__ import annotations
 

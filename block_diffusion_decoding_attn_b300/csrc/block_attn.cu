@@ -4,7 +4,7 @@
 // L keys], with no mask inside the block and GQA head sharing.
 //
 // The causal variant (p.causal) is the context tower's pass over a committed
-// block (Section 2.1, Algorithm 1, "update AR context"): block query l sees
+// block (Section 2.1, Algorithm 1, the context update after a commit): block query l sees
 // the context and block keys 0..l only. The block tiles are masked per row;
 // a row with no visible key in a split (a block tile past it) keeps m = -inf,
 // a zero sum and zero P there, and the merge gives such a split weight 0.

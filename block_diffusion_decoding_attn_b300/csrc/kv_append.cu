@@ -1,5 +1,5 @@
 // Context-tower cache update after a block is committed ("Nemotron-Labs-TwoTower",
-// Section 2.1, Algorithm 1, "update AR context"): the committed block's keys
+// Section 2.1, Algorithm 1, the context update after a commit): the committed block's keys
 // and values of this layer join the prefix cache behind the positions already
 // there, and the cache length grows by L.
 //

@@ -117,8 +117,8 @@ int tt_block_attn(tt_handle handle, const tt_attn_desc* desc, const void* q, con
                   void* stream);
 
 /* ------------------------------------------------------------------------
- * Context-tower update after a commit -- Section 2.1, Algorithm 1, step 8
- * ("update AR context"): once a block is clean, the context tower runs its
+ * Context-tower update after a commit -- Section 2.1, Algorithm 1: once a
+ * block is clean, the context tower runs its
  * tokens causally over the prefix cache and the block's keys/values join the
  * cache. Per attention layer that is tt_block_attn_causal followed by
  * tt_kv_append.

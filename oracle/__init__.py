@@ -18,7 +18,7 @@ method's arithmetic.
   before it and bidirectionally to itself (a loop over blocks of
   ``block_attn``).
 * ``block_attn(..., causal=True)`` and ``kv_append`` follow Section 2.1,
-  Algorithm 1, "update AR context": the context tower's causal pass over a
+  Algorithm 1 (the context update after a commit): the context tower's causal pass over a
   committed block, and its keys/values joining the prefix cache.
 """
 from __future__ import annotations
@@ -154,7 +154,7 @@ def block_attn_train(q, k_noisy, v_noisy, k_clean, v_clean, S, scale=None, rows=
 
 
 def kv_append(k_blk, v_blk, k_ctx, v_ctx, ctx_len):
-    """The cache after a committed block joins it (Algorithm 1, "update AR context").
+    """The cache after a committed block joins it (Section 2.1, Algorithm 1).
 
     k_blk/v_blk [B][L][Hkv][D], k_ctx/v_ctx [B][Hkv][C_cap][D] (any element
     type), ctx_len [B]. Returns new (k_ctx, v_ctx, ctx_len, fits): for every b

@@ -16,8 +16,8 @@
  * positions.
  *
  * Causal variant (tt_oracle_block_attn_causal): the context tower's pass
- * over a committed block (Section 2.1, Algorithm 1, "update AR context": the
- * context tower processes the committed tokens causally). Block query l
+ * over a committed block (Section 2.1, Algorithm 1: once a block is committed,
+ * the context tower runs its tokens causally to update its caches). Block query l
  * takes its softmax over the cache positions and block keys 0..l only, i.e.
  * the key list above cut after block key l.
  *

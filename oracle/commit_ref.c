@@ -154,8 +154,8 @@ int tt_oracle_commit(const float* logits, int B, int L, long V, const uint8_t* m
 }
 
 /*
- * Confidence above a threshold (Section 2.2, Algorithm 2, "predictions above
- * gamma are committed"): confidence = 2^40 / key, so conf > gamma is
+ * Confidence above a threshold (Section 2.2, Algorithm 2: a prediction whose
+ * confidence exceeds gamma is committed): confidence = 2^40 / key, so conf > gamma is
  * gamma * key < 2^40, decided in exact arithmetic. gamma = f * 2^e with f in
  * [0.5, 1), and m = f * 2^53 is an integer, so the test is
  * m * key < 2^(93 - e) on 128-bit integers.

@@ -1,6 +1,6 @@
 """GPU parity of the context-tower update: tt_block_attn_causal and tt_kv_append.
 
-"Nemotron-Labs-TwoTower" Section 2.1, Algorithm 1, "update AR context": the
+"Nemotron-Labs-TwoTower" Section 2.1, Algorithm 1 (the context update after a commit): the
 committed block's tokens run causally over the prefix cache (query l sees the
 cache and block keys 0..l), then the block's keys/values join the cache.
 Acceptance: attention within 1e-2 * max |oracle| (as for tt_block_attn); the

@@ -1,6 +1,6 @@
 """Pins of the oracle's context-tower update: causal block attention and K/V append.
 
-"Nemotron-Labs-TwoTower" Section 2.1, Algorithm 1, step 8 ("update AR context"):
+"Nemotron-Labs-TwoTower" Section 2.1, Algorithm 1 (the context update after a commit):
 once a block is clean the context tower runs its tokens causally over the prefix
 cache, and the block's keys/values join that cache. The checks:
 
