@@ -62,6 +62,8 @@ def _load():
             lib.tt_oracle_block_attn_causal.argtypes = lib.tt_oracle_block_attn.argtypes
             lib.tt_oracle_exp_own.restype = ctypes.c_float
             lib.tt_oracle_exp_own.argtypes = [ctypes.c_float]
+            lib.tt_oracle_exp_n.restype = ctypes.c_float
+            lib.tt_oracle_exp_n.argtypes = [ctypes.c_float]
             lib.tt_oracle_quant.restype = ctypes.c_uint64
             lib.tt_oracle_quant.argtypes = [ctypes.c_float]
             lib.tt_oracle_row_key.restype = None
@@ -184,6 +186,11 @@ def kv_append(k_blk, v_blk, k_ctx, v_ctx, ctx_len):
 def exp_own(x: float) -> float:
     """The fp32 exponential that defines the canonical confidence key."""
     return _load().tt_oracle_exp_own(float(np.float32(x)))
+
+
+def exp_n(x: float) -> int:
+    """The integer n of the exponential's range reduction for x (x ~ n ln 2 + r)."""
+    return int(_load().tt_oracle_exp_n(float(np.float32(x))))
 
 
 def quant(x: float) -> int:

@@ -45,12 +45,21 @@ static const float C1_F = (float)LN2_D;
 
 static float c2_f(void) { return (float)(LN2_D - (double)C1_F); }
 
-/* n = nearest integer (ties to even) to the exact product x * LOG2E; |n| < 2^22. */
+/* n = nearest integer (ties to even) to the exact product x * LOG2E; |n| < 2^22.
+ * This is the Cody-Waite choice of n: the integer nearest to x / ln 2 as
+ * approximated by x * RN32(1/ln 2), rounded once. Rounding the product to fp32
+ * first and then to an integer would round twice; the two differ for x whose
+ * product lies within half an fp32 ulp of a half-integer (e.g. x = -1.0397208,
+ * where RN32(x * LOG2E) = -1.5 exactly and the exact product is above it). */
 static float reduce_n(float x) {
     const float magic = 12582912.0f; /* 1.5 * 2^23: sums in [2^23, 2^24) have ulp 1 */
     const float nb = fmaf(x, LOG2E_F, magic);
     return nb - magic;
 }
+
+/* The n of the reduction step for x (exposed so that the tests can pin which
+ * rounding defines it). */
+float tt_oracle_exp_n(float x) { return reduce_n(x); }
 
 /* e(x) for -30 <= x <= 0 as a float: p(r) * 2^n. Returns 0 below -30. */
 float tt_oracle_exp_own(float x) {

@@ -52,6 +52,76 @@ def test_own_exp_against_libm(oracle_lib):
     assert oracle_lib.exp_own(-30.5) == 0.0
 
 
+def _rhe(q: Fraction) -> int:
+    """Round a rational to the nearest integer, ties to even."""
+    fl = math.floor(q)
+    fr = q - fl
+    return fl + (1 if fr > Fraction(1, 2) or (fr == Fraction(1, 2) and fl % 2) else 0)
+
+
+def _rn32(q: Fraction) -> Fraction:
+    """Round a nonzero rational in the fp32 normal range to fp32, ties to even (exact)."""
+    if q == 0:
+        return Fraction(0)
+    s = -1 if q < 0 else 1
+    a = abs(q)
+    e = math.floor(math.log2(a))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (e - 23)
+    return s * _rhe(a / ulp) * ulp
+
+
+def _quant_from_definition(x: float, n: int) -> int:
+    """rint(2^40 * p(r) * 2^n) for a given n, every fp32 step done in exact
+    rational arithmetic with one rounding per fused multiply-add."""
+    ln2 = Fraction(0.69314718055994530942)   # the double nearest ln 2
+    c1 = _rn32(ln2)
+    c2 = _rn32(ln2 - c1)
+    r = _rn32(-n * c1 + Fraction(x))
+    r = _rn32(-n * c2 + r)
+    c = [_rn32(1 / Fraction(math.factorial(j))) for j in range(8)]
+    p = c[7]
+    for j in range(6, -1, -1):
+        p = _rn32(p * r + c[j])
+    return _rhe(p * Fraction(2) ** (n + 40))
+
+
+def test_reduction_n_is_one_rounding_of_the_exact_product(oracle_lib):
+    # The reduction's n is the integer nearest the exact product x * RN32(1/ln 2),
+    # rounded once (the Cody-Waite reduction as done with an FMA and a
+    # 1.5 * 2^23 shifter, Muller, "Elementary Functions", Ch. 11). These x are
+    # the fp32 values in [-30, 0] where rounding the product to fp32 first and
+    # then to an integer gives another n: the product lies within half an fp32
+    # ulp of a half-integer. The pin fixes the documented n, and the key term
+    # that follows from it, against exact rational arithmetic.
+    l2e = Fraction(float(np.float32(1.0 / 0.69314718055994530942)))
+    cases = []
+    for k in range(44):
+        x0 = np.float32(-(k + 0.5) / float(l2e))
+        for d in range(-40, 41):
+            x = np.array([x0.view(np.int32) + d], np.int32).view(np.float32)[0]
+            if not (-30.0 <= x <= 0.0):
+                continue
+            n_exact = _rhe(Fraction(float(x)) * l2e)
+            n_twice = int(np.rint(np.float32(x) * np.float32(l2e)))  # RN32, then rint
+            if n_exact != n_twice:
+                cases.append((float(x), n_exact, n_twice))
+    assert len(cases) >= 20
+    assert any(x == float(np.float32(-1.0397208)) for x, _, _ in cases)
+    differs = 0
+    for x, n_exact, n_twice in cases:
+        assert oracle_lib.exp_n(x) == n_exact, x
+        q = oracle_lib.quant(x)
+        assert q == _quant_from_definition(x, n_exact), x
+        differs += q != _quant_from_definition(x, n_twice)
+        # either way the term stays within the exponential's error bound
+        assert abs(q - TWO40 * math.exp(x)) <= TWO40 * math.exp(x) * 2.0 ** -22 + 1
+    assert differs >= 1  # the key terms themselves tell the two readings apart
+
+
 def test_quantiser_is_exact_rounding_of_scaled_exp(oracle_lib):
     rng = np.random.default_rng(0)
     xs = np.concatenate([-rng.random(3000) * 30, -rng.random(500) * 1e-3, [0.0, -29.9, -30.0]])
