@@ -37,7 +37,8 @@ import numpy as np  # noqa: E402
 
 from block_diffusion_decoding_attn_b300 import workload as wl  # noqa: E402
 
-DEFAULT_WORKLOAD = "b8_c4096_l32"
+DEFAULT_WORKLOAD = "b64_ragged8k32k_l64"  # the largest single-GPU workload
+SCHEDULE_WORKLOAD = "b4_gen8k_32x256"     # reported beside it under kernels
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -212,7 +213,8 @@ def config_of(w, inps):
          "commit_state": "fully masked block (first denoising step)",
          "l2": "flushed before every call, outside the timed events: a 256 MiB write, then a "
                "read of the same buffer so that no dirty line is left to be written back "
-               "inside the timed region"}
+               "inside the timed region; then a 0.2 ms GPU spin so that the call is queued "
+               "before its start event is reached"}
     return c
 
 
@@ -325,6 +327,113 @@ def attn_calls(w, seed):
     return calls
 
 
+def gpu_calls(w, dev, seed, pin=True):
+    """Device tensors of one step of workload w: per attention call a dict of
+    q / k_blk / v_blk / ctx_len plus the shared context cache, and the commit
+    inputs. Returns (inps, calls, cache, cinp, commit tensors)."""
+    inps = attn_calls(w, seed=seed)
+    cinp = wl.commit_inputs(w, seed=seed)
+    cache = wl.attn_tensors(inps[-1], dev, pin=pin)  # context cache shared by all calls
+    calls = []
+    for inp in inps:
+        if inp is inps[-1]:
+            calls.append(cache)
+            continue
+        t = wl.attn_tensors(wl.AttnInputs(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx[:0], inp.v_ctx[:0],
+                                          inp.ctx_len, inp.scale), dev, pin=pin)
+        t["k_ctx"], t["v_ctx"] = cache["k_ctx"], cache["v_ctx"]
+        calls.append(t)
+    Cm = wl.commit_tensors(cinp, dev, pin=pin)
+    return inps, calls, cache, cinp, Cm
+
+
+class L2Flush:
+    """Evicts everything from the 126 MB L2 between timed calls. The write alone
+    would leave up to an L2's worth of dirty lines whose write-back then runs
+    inside the next timed call; reading the buffer afterwards replaces them
+    with clean lines. A short spin on the GPU follows, so that the host has
+    queued the timed call (and its start event) before the GPU reaches them:
+    otherwise the events would also time the GPU waiting for the launch."""
+
+    SPIN_CYCLES = 400_000  # about 0.2 ms at 2 GHz, more than a call's host time
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        import torch
+        self.buf.zero_()
+        self.sink.copy_(self.buf.view(torch.int64).sum())
+        torch.cuda._sleep(self.SPIN_CYCLES)
+
+
+def time_schedule(tt, h, stream, flush, w, calls, Cm, out, m_out, rounds, warm):
+    """Per round, the summed device time of every call's attention and of its
+    commit (fully masked block), each of the two after an L2 flush."""
+    import torch
+
+    def one(A, e=None):
+        flush()
+        if e:
+            e[0].record(stream)
+        tt.block_attn(A["q"], A["k_blk"], A["v_blk"], A["k_ctx"], A["v_ctx"], A["ctx_len"],
+                      out=out, h=h, stream=stream)
+        if e:
+            e[1].record(stream)
+        flush()
+        if e:
+            e[2].record(stream)
+        tt.commit(Cm["logits"], w.B, w.L, Cm["masked"], w.k, Cm["tok"], masked_out=m_out, h=h,
+                  stream=stream)
+        if e:
+            e[3].record(stream)
+
+    for _ in range(warm):
+        for A in calls:
+            one(A)
+    torch.cuda.synchronize()
+    if h.get_error():
+        raise RuntimeError("device status set during warm-up")
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in calls]
+          for _ in range(rounds)]
+    for i in range(rounds):
+        for j, A in enumerate(calls):
+            one(A, ev[i][j])
+    torch.cuda.synchronize()
+    st = h.get_error()
+    if st:
+        raise RuntimeError(f"device status {st} during the timed region")
+    t_attn = [sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for j in range(len(calls)))
+              for i in range(rounds)]
+    t_comm = [sum(ev[i][j][2].elapsed_time(ev[i][j][3]) for j in range(len(calls)))
+              for i in range(rounds)]
+    return t_attn, t_comm
+
+
+def roof_attention(w, inps, a_ms, peaks, name):
+    ncalls = len(inps)
+    fl = sum(attn_flops(w, inp.ctx_len) for inp in inps) / ncalls
+    by = sum(attn_bytes(w, inp.ctx_len) for inp in inps) / ncalls
+    tf = fl / (a_ms * 1e-3) / 1e12
+    per = "per call" if ncalls == 1 else f"per call, mean over the {ncalls} calls of a step"
+    return {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": tf / peaks["bf16_tflops"], "traffic": profiled_traffic("block_attn", name),
+            "kernel": "tt_block_attn call (one persistent attention kernel, pieces merged in it)",
+            "algorithmic": f"{fl:.4g} FLOP, {by:.4g} B {per}", "ms": a_ms,
+            "peak_source": peaks["source"] + " burst"}
+
+
+def roof_commit(w, masked_rows, c_ms, peaks, name, what="per call"):
+    by = commit_bytes(w, masked_rows)
+    gbs = by / (c_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "traffic": profiled_traffic("commit", name),
+            "kernel": "tt_commit call (row reduction + top-k select, one launch)",
+            "algorithmic": f"{by:.4g} B {what}", "ms": c_ms, "peak_source": peaks["source"]}
+
+
 def run_gpu(args, w):
     import torch
     import block_diffusion_decoding_attn_b300 as tt
@@ -344,90 +453,63 @@ def run_gpu(args, w):
     if dist:
         dist.barrier()
     h = tt.handle(local)
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev)
+    peaks = load_peaks()
 
     # inputs resident in HBM before timing (each rank its own batch)
-    inps = attn_calls(w, seed=rank)
-    cinp = wl.commit_inputs(w, seed=rank)
-    cache = wl.attn_tensors(inps[-1], dev, pin=True)  # context cache shared by all calls
-    As = []
-    for inp in inps:
-        if inp is inps[-1]:
-            As.append(cache)
-            continue
-        t = wl.attn_tensors(wl.AttnInputs(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx[:0], inp.v_ctx[:0],
-                                          inp.ctx_len, inp.scale), dev, pin=True)
-        t["k_ctx"], t["v_ctx"] = cache["k_ctx"], cache["v_ctx"]
-        As.append(t)
-    Cm = wl.commit_tensors(cinp, dev, pin=True)
+    inps, As, cache, cinp, Cm = gpu_calls(w, dev, seed=rank)
     out = torch.empty_like(As[0]["q"])
     m_out = torch.empty_like(Cm["masked"])
-    desc = tt.attn_desc(As[0]["q"], As[0]["k_ctx"])
-    ws_a_n = tt.block_attn_workspace_bytes(desc, h)
-    ws_a = torch.empty(max(ws_a_n, 256), dtype=torch.uint8, device=dev)
-    ws_c = torch.zeros(max(tt.commit_workspace_bytes(w.B, w.L), 256), dtype=torch.uint8,
-                       device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_sum = torch.empty((), dtype=torch.int64, device=dev)
+    h.reserve(tt.attn_desc(As[0]["q"], As[0]["k_ctx"]), w.B, w.L)  # no allocation while timing
     ncalls = len(As)
-
-    def flush_l2():
-        # Evicts the step's inputs from the 126 MB L2. The write alone would
-        # leave up to an L2's worth of dirty lines whose write-back then runs
-        # inside the next timed step; reading the buffer afterwards replaces
-        # them with clean lines.
-        flush.zero_()
-        flush_sum.copy_(flush.view(torch.int64).sum())
-
-    stream = torch.cuda.current_stream(dev)
-    # per call: attention (+ split merge) + commit
-    launches_per_step = ncalls * (1 + (1 if ws_a_n > 0 else 0) + 1)
-
-    def attention(A):
-        tt.block_attn(A["q"], A["k_blk"], A["v_blk"], A["k_ctx"], A["v_ctx"], A["ctx_len"],
-                      out=out, workspace=ws_a, h=h, stream=stream)
-
-    def commit():
-        tt.commit(Cm["logits"], w.B, w.L, Cm["masked"], w.k, Cm["tok"], masked_out=m_out,
-                  workspace=ws_c, h=h, stream=stream)
-
-    for _ in range(max(args.warmup, 3)):
-        for A in As:
-            flush_l2()
-            attention(A)
-            commit()
-    torch.cuda.synchronize()
-    if h.get_error():
-        raise RuntimeError("device status set during warm-up")
+    launches_per_step = ncalls * 2  # one attention and one commit launch per call
 
     K = args.steps
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(ncalls)]
-          for _ in range(K)]
     with ClockSampler(local) as clk:
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
-        for i in range(K):
-            for j, A in enumerate(As):
-                flush_l2()  # every call starts from a cold L2
-                e0, e1, e2 = ev[i][j]
-                e0.record(stream)
-                attention(A)
-                e1.record(stream)
-                commit()
-                e2.record(stream)
-        torch.cuda.synchronize()
+        t_attn, t_comm = time_schedule(tt, h, stream, flush, w, As, Cm, out, m_out, K,
+                                       max(args.warmup, 3))
         wall = time.perf_counter() - wall0
         if dist:
             dist.barrier()
-    st = h.get_error()
-    if st:
-        raise RuntimeError(f"device status {st} during the timed region")
-    t_attn = [sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for j in range(ncalls)) for i in range(K)]
-    t_comm = [sum(ev[i][j][1].elapsed_time(ev[i][j][2]) for j in range(ncalls)) for i in range(K)]
     ms_step = max_over_ranks((sum(t_attn) + sum(t_comm)) / K, dist)
     tokens = tokens_per_step(w, ncalls, world)
     value = tokens / (ms_step * 1e-3)
+
+    # The commit over a whole block's denoising (T = ceil(L/k) steps, k commits
+    # per block per step): the masks of every step come from one untimed run of
+    # the loop; each step reads only its still-masked rows (the step-1 logits
+    # are reused, which changes no byte count).
+    T = w.steps_to_unmask
+    masks = []
+    mk = torch.ones_like(Cm["masked"])
+    tk = torch.full_like(Cm["tok"], -1)
+    for s in range(T):
+        masks.append(mk.clone())
+        tt.commit(Cm["logits"], w.B, w.L, mk, w.k, tk, masked_out=mk, h=h, stream=stream)
+    torch.cuda.synchronize()
+    mbuf = torch.empty_like(Cm["masked"])
+    Kl = max(3, min(K, 10))
+    evl = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(T)]
+           for _ in range(Kl + 1)]
+    for i in range(Kl + 1):  # the first round warms up
+        for s in range(T):
+            mbuf.copy_(masks[s])
+            flush()
+            evl[i][s][0].record(stream)
+            tt.commit(Cm["logits"], w.B, w.L, mbuf, w.k, tk, masked_out=m_out, h=h, stream=stream)
+            evl[i][s][1].record(stream)
+    torch.cuda.synchronize()
+    if h.get_error():
+        raise RuntimeError("device status set during the commit-loop leg")
+    loop_ms = statistics.mean(sum(evl[i][s][0].elapsed_time(evl[i][s][1]) for s in range(T))
+                              for i in range(1, Kl + 1))
+    loop_ms = max_over_ranks(loop_ms, dist)
+    loop_rows = [int(m.sum().item()) for m in masks]
 
     # End to end through the public API: host (pinned) buffers in, results
     # out. Per step: the context cache once, every call's block tensors and
@@ -456,10 +538,9 @@ def run_gpu(args, w):
             for k, v in host_commit.items():
                 dev_commit[k].copy_(v, non_blocking=True)
             tt.block_attn(dev_call["q"], dev_call["k_blk"], dev_call["v_blk"], dev_cache["k_ctx"],
-                          dev_cache["v_ctx"], dev_call["ctx_len"], out=out, workspace=ws_a, h=h,
-                          stream=stream)
+                          dev_cache["v_ctx"], dev_call["ctx_len"], out=out, h=h, stream=stream)
             tt.commit(dev_commit["logits"], w.B, w.L, dev_commit["masked"], w.k,
-                      dev_commit["tok"], masked_out=m_out, workspace=ws_c, h=h, stream=stream)
+                      dev_commit["tok"], masked_out=m_out, h=h, stream=stream)
             host_out["out"].copy_(out, non_blocking=True)
             host_out["tok"].copy_(dev_commit["tok"], non_blocking=True)
             host_out["masked"].copy_(m_out, non_blocking=True)
@@ -473,6 +554,7 @@ def run_gpu(args, w):
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks((time.perf_counter() - te0) / Ke * 1e3, dist)
+    del dev_cache, dev_call, dev_commit, host_cache, host_calls, host_commit
 
     # Context-tower update, once per committed block (not part of the step):
     # the causal pass over (cache, block) then the block's K/V appended. It
@@ -484,13 +566,10 @@ def run_gpu(args, w):
     for k in big:
         big[k][:, :, :cap_].copy_(cache[k])
     n_run = torch.empty_like(As[0]["ctx_len"])
-    desc_u = tt.attn_desc(As[0]["q"], big["k_ctx"])
-    ws_u = torch.empty(max(tt.block_attn_workspace_bytes(desc_u, h), 256), dtype=torch.uint8,
-                       device=dev)
 
     def update(A):
         tt.block_attn(A["q"], A["k_blk"], A["v_blk"], big["k_ctx"], big["v_ctx"], n_run, out=out,
-                      workspace=ws_u, h=h, stream=stream, causal=True)
+                      h=h, stream=stream, causal=True)
         tt.kv_append(A["k_blk"], A["v_blk"], big["k_ctx"], big["v_ctx"], n_run, h=h, stream=stream)
 
     Ku = max(3, min(K, 10))
@@ -499,7 +578,7 @@ def run_gpu(args, w):
     for i in range(Ku + 2):  # the first two rounds warm up
         for j, A in enumerate(As):
             n_run.copy_(A["ctx_len"])
-            flush_l2()
+            flush()
             evu[i][j][0].record(stream)
             update(A)
             evu[i][j][1].record(stream)
@@ -516,56 +595,65 @@ def run_gpu(args, w):
     wt = wl.custom("train", TRAIN_B, TRAIN_N, w.Hq, w.Hkv, w.D, TRAIN_N, (TRAIN_N,) * TRAIN_B)
     Tt = wl.attn_tensors(wl.attn_inputs(wt, seed=rank), dev)
     out_t = torch.empty_like(Tt["q"])
-
-    def train_attn():
-        tt.block_attn_train(Tt["q"], Tt["k_blk"], Tt["v_blk"], Tt["k_ctx"], Tt["v_ctx"], TRAIN_S,
-                            out=out_t, h=h, stream=stream)
-
     evt = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ku + 2)]
     for i in range(Ku + 2):  # the first two warm up
-        flush_l2()
+        flush()
         evt[i][0].record(stream)
-        train_attn()
+        tt.block_attn_train(Tt["q"], Tt["k_blk"], Tt["v_blk"], Tt["k_ctx"], Tt["v_ctx"], TRAIN_S,
+                            out=out_t, h=h, stream=stream)
         evt[i][1].record(stream)
     torch.cuda.synchronize()
     if h.get_error():
         raise RuntimeError("device status set during the training-attention leg")
     tr_ms = max_over_ranks(statistics.mean(evt[i][0].elapsed_time(evt[i][1])
                                            for i in range(2, Ku + 2)), dist)
-    del Tt
+    del Tt, out_t
+
+    # The 8K-token generation schedule (32 calls, context growing by one
+    # block each call), per-call attention and commit, when it is not the
+    # step's own workload.
+    sched = None
+    if w.name != SCHEDULE_WORKLOAD:
+        ws = wl.WORKLOADS[SCHEDULE_WORKLOAD]
+        s_inps, s_As, _, s_cinp, s_Cm = gpu_calls(ws, dev, seed=rank, pin=False)
+        s_out = torch.empty_like(s_As[0]["q"])
+        s_mout = torch.empty_like(s_Cm["masked"])
+        h.reserve(tt.attn_desc(s_As[0]["q"], s_As[0]["k_ctx"]), ws.B, ws.L)
+        Ks = max(2, min(K, 5))
+        sa, sc = time_schedule(tt, h, stream, flush, ws, s_As, s_Cm, s_out, s_mout, Ks, 1)
+        n_s = len(s_As)
+        sa_ms = max_over_ranks(statistics.mean(sa) / n_s, dist)
+        sc_ms = max_over_ranks(statistics.mean(sc) / n_s, dist)
+        sched = {"workload": ws.name, "calls": n_s, "rounds": Ks,
+                 "attention": roof_attention(ws, s_inps, sa_ms, peaks, ws.name),
+                 "commit": roof_commit(ws, int(s_cinp.masked.sum()), sc_ms, peaks, ws.name),
+                 "block_tokens_per_s": ws.B * ws.L / ((sa_ms + sc_ms) * 1e-3)}
+        del s_As, s_Cm, s_out, s_mout
 
     if rank != 0:
         dist.destroy_process_group() if dist else None
         return 0
 
-    peaks = load_peaks()
     a_ms, c_ms = statistics.mean(t_attn) / ncalls, statistics.mean(t_comm) / ncalls  # per call
-    fl = sum(attn_flops(w, inp.ctx_len) for inp in inps) / ncalls
-    by_a = sum(attn_bytes(w, inp.ctx_len) for inp in inps) / ncalls
-    by_c = commit_bytes(w, int(cinp.masked.sum()))
-    attn_tf = fl / (a_ms * 1e-3) / 1e12
-    comm_gbs = by_c / (c_ms * 1e-3) / 1e9
-    per = "per call" if ncalls == 1 else f"per call, mean over the {ncalls} calls of a step"
-    roof_attn = {"bound": "tensor", "achieved": attn_tf, "peak": peaks["bf16_tflops"],
-                 "unit": "TFLOP/s", "frac": attn_tf / peaks["bf16_tflops"],
-                 "traffic": profiled_traffic("block_attn", w.name),
-                 "kernel": "tt_block_attn call (attention kernel + split merge)",
-                 "algorithmic": f"{fl:.4g} FLOP, {by_a:.4g} B {per}",
-                 "ms": a_ms, "peak_source": peaks["source"] + " burst"}
-    roof_comm = {"bound": "hbm", "achieved": comm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                 "frac": comm_gbs / peaks["hbm_gbs"],
-                 "traffic": profiled_traffic("commit", w.name),
-                 "kernel": "tt_commit call (row reduction + top-k select)",
-                 "algorithmic": f"{by_c:.4g} B {per}", "ms": c_ms,
-                 "peak_source": peaks["source"]}
+    roof_attn = roof_attention(w, inps, a_ms, peaks, w.name)
+    roof_comm = roof_commit(w, int(cinp.masked.sum()), c_ms, peaks, w.name)
+    loop_bytes = sum(commit_bytes(w, r) for r in loop_rows)
+    loop_gbs = loop_bytes / (loop_ms * 1e-3) / 1e9
+    roof_loop = {"bound": "hbm", "achieved": loop_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": loop_gbs / peaks["hbm_gbs"], "traffic": None,
+                 "kernel": f"tt_commit over the {T} steps of a block's denoising "
+                           f"(k = {w.k}; masked rows per step {loop_rows})",
+                 "algorithmic": f"{loop_bytes:.4g} B per loop", "ms": loop_ms,
+                 "ms_per_step": loop_ms / T, "peak_source": peaks["source"]}
     fl_u = sum(causal_flops(w, inp.ctx_len) for inp in inps) / ncalls
+    by_a = sum(attn_bytes(w, inp.ctx_len) for inp in inps) / ncalls
     by_u = by_a + append_bytes(w)
     upd_tf = fl_u / (u_ms * 1e-3) / 1e12
     roof_upd = {"bound": "tensor", "achieved": upd_tf, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": upd_tf / peaks["bf16_tflops"], "traffic": None,
                 "kernel": "context-tower update per committed block: tt_block_attn_causal "
-                          "(+ split merge) then tt_kv_append; outside the step",
-                "algorithmic": f"{fl_u:.4g} FLOP (unmasked pairs), {by_u:.4g} B {per}",
+                          "then tt_kv_append; outside the step",
+                "algorithmic": f"{fl_u:.4g} FLOP (unmasked pairs), {by_u:.4g} B per call",
                 "ms": u_ms, "block_tokens_per_s": w.B * w.L / (u_ms * 1e-3),
                 "peak_source": peaks["source"] + " burst"}
     fl_t = train_flops(w, TRAIN_B, TRAIN_N, TRAIN_S)
@@ -579,6 +667,10 @@ def run_gpu(args, w):
                   "ms": tr_ms, "tokens_per_s": TRAIN_B * TRAIN_N / (tr_ms * 1e-3),
                   "peak_source": peaks["source"] + " burst"}
     dom = roof_attn if a_ms >= c_ms else roof_comm
+    kernels = {"attention": roof_attn, "commit": roof_comm, "commit_full_loop": roof_loop,
+               "context_update": roof_upd, "train_attention": roof_train}
+    if sched:
+        kernels[SCHEDULE_WORKLOAD] = sched
     line = {
         "metric": "denoised block-tokens/s per layer-step", "value": value,
         "unit": "block-tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -587,8 +679,7 @@ def run_gpu(args, w):
         "data": "synthetic (seeded Philox normals; inputs resident in HBM)",
         "config": config_of(w, inps),
         "roofline": dom,
-        "kernels": {"attention": roof_attn, "commit": roof_comm, "context_update": roof_upd,
-                    "train_attention": roof_train},
+        "kernels": kernels,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "block-tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": Ke},

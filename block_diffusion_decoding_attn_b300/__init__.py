@@ -31,6 +31,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtt.so")
 
 TT_OK = 0
+TT_ERR_INVALID_ARG, TT_ERR_UNSUPPORTED, TT_ERR_CUDA, TT_ERR_TIMEOUT, TT_ERR_DEVICE_CHECK = (
+    -1, -2, -3, -4, -5)
 TT_DEV_CTX_LEN_RANGE = 1
 TT_DEV_WAIT_TIMEOUT = 2
 
@@ -56,29 +58,31 @@ def lib() -> ctypes.CDLL:
                 raise ImportError(f"{LIB_PATH} is missing: run block_diffusion_decoding_attn_b300."
                                   "build.build() (nvcc, sm_103a) first")
             L = ctypes.CDLL(LIB_PATH)
-            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            P, I = ctypes.c_void_p, ctypes.c_int
             L.tt_create.argtypes = [ctypes.POINTER(P), I]
             L.tt_destroy.argtypes = [P]
-            L.tt_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+            L.tt_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
             L.tt_set_wait_timeout.argtypes = [P, ctypes.c_ulonglong]
+            L.tt_set_attn_schedule.argtypes = [P, I, I, I, I]
+            L.tt_reserve.argtypes = [P, ctypes.POINTER(AttnDesc), I, I]
             L.tt_status_string.restype = ctypes.c_char_p
             L.tt_status_string.argtypes = [I]
             L.tt_last_error.restype = ctypes.c_char_p
             L.tt_last_error.argtypes = []
-            L.tt_block_attn_workspace_bytes.restype = S
-            L.tt_block_attn_workspace_bytes.argtypes = [P, ctypes.POINTER(AttnDesc)]
-            L.tt_block_attn.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 7 + [P, S, P]
+            L.tt_block_attn.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 7 + [P]
             L.tt_block_attn_causal.argtypes = L.tt_block_attn.argtypes
             L.tt_kv_append.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 5 + [P]
-            L.tt_block_attn_train_workspace_bytes.restype = S
-            L.tt_block_attn_train_workspace_bytes.argtypes = [P, ctypes.POINTER(TrainDesc)]
-            L.tt_block_attn_train.argtypes = [P, ctypes.POINTER(TrainDesc)] + [P] * 6 + [P, S, P]
-            L.tt_commit_workspace_bytes.restype = S
-            L.tt_commit_workspace_bytes.argtypes = [I, I]
-            L.tt_commit.argtypes = [P, P, I, I, I, P, I, P, P, P, S, P]
-            L.tt_commit_threshold.argtypes = [P, P, I, I, I, P, ctypes.c_double, I, P, P, P, S, P]
+            L.tt_block_attn_train.argtypes = [P, ctypes.POINTER(TrainDesc)] + [P] * 6 + [P]
+            L.tt_commit.argtypes = [P, P, I, I, I, P, I, P, P, P]
+            L.tt_commit_threshold.argtypes = [P, P, I, I, I, P, ctypes.c_double, I, P, P, P]
+            L.tt_commit_keys.argtypes = [P, P, P, I, P]
+            L.tt_commit_noalloc.argtypes = [P, I, I, I, P, I, P, P, P]
+            L.tt_commit_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
             for f in ("tt_create", "tt_destroy", "tt_get_error", "tt_set_wait_timeout",
-                      "tt_block_attn", "tt_commit", "tt_commit_threshold"):
+                      "tt_set_attn_schedule", "tt_reserve", "tt_block_attn",
+                      "tt_block_attn_causal", "tt_kv_append", "tt_block_attn_train", "tt_commit",
+                      "tt_commit_threshold", "tt_commit_keys", "tt_commit_noalloc",
+                      "tt_commit_noalloc_status"):
                 getattr(L, f).restype = I
             _lib = L
     return _lib
@@ -87,13 +91,13 @@ def lib() -> ctypes.CDLL:
 class AttnDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("Hq", ctypes.c_int),
                 ("Hkv", ctypes.c_int), ("D", ctypes.c_int), ("ctx_cap", ctypes.c_int),
-                ("scale", ctypes.c_float), ("num_splits", ctypes.c_int)]
+                ("scale", ctypes.c_float)]
 
 
 class TrainDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("S", ctypes.c_int),
                 ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
-                ("scale", ctypes.c_float), ("num_splits", ctypes.c_int)]
+                ("scale", ctypes.c_float)]
 
 
 def _check(status: int, what: str):
@@ -117,14 +121,27 @@ class Handle:
 
     def get_error(self) -> int:
         """Synchronizes the device; returns and clears the TT_DEV_* status bits."""
-        st = ctypes.c_uint(0)
+        st = ctypes.c_int(0)
         rc = lib().tt_get_error(self._h, ctypes.byref(st))
-        if rc not in (TT_OK, -4):
+        if rc not in (TT_OK, TT_ERR_TIMEOUT, TT_ERR_DEVICE_CHECK):
             _check(rc, "tt_get_error")
         return st.value
 
     def set_wait_timeout(self, ns: int):
         _check(lib().tt_set_wait_timeout(self._h, int(ns)), "tt_set_wait_timeout")
+
+    def set_attn_schedule(self, kernel: int = 0, max_ctas: int = 0, min_tiles: int = 0,
+                          splits: int = 0):
+        """Attention schedule (tt_set_attn_schedule): kernel 0 by shape, 1 one
+        unit per CTA, 2 persistent; max_ctas / min_tiles for the persistent
+        schedule; splits for the one-unit-per-CTA schedule (0 = defaults)."""
+        _check(lib().tt_set_attn_schedule(self._h, int(kernel), int(max_ctas), int(min_tiles),
+                                          int(splits)), "tt_set_attn_schedule")
+
+    def reserve(self, attn: "AttnDesc | None" = None, commit_B: int = 0, commit_L: int = 0):
+        """Grows the handle's scratch for these shapes now (so calls do not allocate)."""
+        _check(lib().tt_reserve(self._h, ctypes.byref(attn) if attn is not None else None,
+                                int(commit_B), int(commit_L)), "tt_reserve")
 
     def close(self):
         if self._h:
@@ -164,20 +181,14 @@ def _dev_ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def attn_desc(q, k_ctx, scale: float = 0.0, num_splits: int = 0) -> AttnDesc:
+def attn_desc(q, k_ctx, scale: float = 0.0) -> AttnDesc:
     B, L, Hq, D = q.shape
     Hkv, C = k_ctx.shape[1], k_ctx.shape[2]
-    return AttnDesc(B, L, Hq, Hkv, D, C, float(scale), int(num_splits))
-
-
-def block_attn_workspace_bytes(desc: AttnDesc, h: Handle | None = None) -> int:
-    h = h or handle()
-    return int(lib().tt_block_attn_workspace_bytes(h.ptr, ctypes.byref(desc)))
+    return AttnDesc(B, L, Hq, Hkv, D, C, float(scale))
 
 
 def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out=None, scale: float = 0.0,
-               num_splits: int = 0, workspace=None, h: Handle | None = None, stream=None,
-               causal: bool = False):
+               h: Handle | None = None, stream=None, causal: bool = False):
     """Block attention, Eq. (1): one softmax per query over [context keys; block keys].
 
     q [B][L][Hq][D], k_blk/v_blk [B][L][Hkv][D], k_ctx/v_ctx [B][Hkv][C_cap][D]
@@ -193,24 +204,18 @@ def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out=None, scale: float = 
     if ctx_len.dtype != torch.int32 or not ctx_len.is_cuda:
         raise ValueError("ctx_len must be an int32 CUDA tensor")
     h = h or handle(q.device.index)
-    desc = attn_desc(q, k_ctx, scale, num_splits)
+    desc = attn_desc(q, k_ctx, scale)
     if out is None:
         out = torch.empty_like(q)
-    need = block_attn_workspace_bytes(desc, h)
-    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    wsp = _dev_ptr(workspace) if need else ctypes.c_void_p(0)
-    wsn = workspace.numel() * workspace.element_size() if need else 0
     fn = lib().tt_block_attn_causal if causal else lib().tt_block_attn
     _check(fn(h.ptr, ctypes.byref(desc), _dev_ptr(q), _dev_ptr(k_blk), _dev_ptr(v_blk),
-              _dev_ptr(k_ctx), _dev_ptr(v_ctx), _dev_ptr(ctx_len), _dev_ptr(out), wsp, wsn,
+              _dev_ptr(k_ctx), _dev_ptr(v_ctx), _dev_ptr(ctx_len), _dev_ptr(out),
               _stream_ptr(q, stream)), "tt_block_attn_causal" if causal else "tt_block_attn")
     return out
 
 
 def block_attn_train(q, k_noisy, v_noisy, k_clean, v_clean, S: int, out=None,
-                     scale: float = 0.0, num_splits: int = 0, workspace=None,
-                     h: Handle | None = None, stream=None):
+                     scale: float = 0.0, h: Handle | None = None, stream=None):
     """Training-time batched block attention (Section 2.3): noisy block j of each
     sequence attends to the clean keys of positions 0..j*S-1 and to its own S
     noisy keys.
@@ -230,17 +235,12 @@ def block_attn_train(q, k_noisy, v_noisy, k_clean, v_clean, S: int, out=None,
             tuple(k_clean.shape) != (B, Hkv, N, D) or tuple(v_clean.shape) != (B, Hkv, N, D):
         raise ValueError("block_attn_train: inconsistent shapes")
     h = h or handle(q.device.index)
-    desc = TrainDesc(B, N, int(S), Hq, Hkv, D, float(scale), int(num_splits))
+    desc = TrainDesc(B, N, int(S), Hq, Hkv, D, float(scale))
     if out is None:
         out = torch.empty_like(q)
-    need = int(lib().tt_block_attn_train_workspace_bytes(h.ptr, ctypes.byref(desc)))
-    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    wsp = _dev_ptr(workspace) if need else ctypes.c_void_p(0)
-    wsn = workspace.numel() * workspace.element_size() if need else 0
     _check(lib().tt_block_attn_train(h.ptr, ctypes.byref(desc), _dev_ptr(q), _dev_ptr(k_noisy),
                                      _dev_ptr(v_noisy), _dev_ptr(k_clean), _dev_ptr(v_clean),
-                                     _dev_ptr(out), wsp, wsn, _stream_ptr(q, stream)),
+                                     _dev_ptr(out), _stream_ptr(q, stream)),
            "tt_block_attn_train")
     return out
 
@@ -264,76 +264,68 @@ def kv_append(k_blk, v_blk, k_ctx, v_ctx, ctx_len, h: Handle | None = None, stre
             k_ctx.shape[3] != D or tuple(v_ctx.shape) != tuple(k_ctx.shape):
         raise ValueError("kv_append: inconsistent shapes")
     h = h or handle(k_blk.device.index)
-    desc = AttnDesc(B, L, Hkv, Hkv, D, int(k_ctx.shape[2]), 0.0, 0)
+    desc = AttnDesc(B, L, Hkv, Hkv, D, int(k_ctx.shape[2]), 0.0)
     _check(lib().tt_kv_append(h.ptr, ctypes.byref(desc), _dev_ptr(k_blk), _dev_ptr(v_blk),
                               _dev_ptr(k_ctx), _dev_ptr(v_ctx), _dev_ptr(ctx_len),
                               _stream_ptr(k_blk, stream)), "tt_kv_append")
     return k_ctx, v_ctx
 
 
-def commit_workspace_bytes(B: int, L: int) -> int:
-    return int(lib().tt_commit_workspace_bytes(int(B), int(L)))
-
-
-def commit(logits, B: int, L: int, masked, k: int, tok, masked_out=None, workspace=None,
-           h: Handle | None = None, stream=None):
-    """One unmask/commit step (Algorithm 2, budget k per block).
-
-    logits [B*L][V] float32, masked [B*L] uint8, tok [B*L] int32 (updated in
-    place at committed rows). Returns (tok, masked_out, workspace); the
-    workspace holds key[B*L] (uint64), arg[B*L] (int32) and the block tickets.
-    A caller-provided workspace must have been zero-filled before its first use.
-    """
+def _check_commit_args(logits, masked, tok):
     import torch
     if logits.dtype != torch.float32 or not logits.is_cuda or not logits.is_contiguous():
         raise ValueError("logits must be a contiguous CUDA float32 tensor")
     if masked.dtype != torch.uint8 or tok.dtype != torch.int32:
         raise ValueError("masked must be uint8 and tok int32")
+
+
+def commit(logits, B: int, L: int, masked, k: int, tok, masked_out=None,
+           h: Handle | None = None, stream=None):
+    """One unmask/commit step (Algorithm 2, budget k per block).
+
+    logits [B*L][V] float32, masked [B*L] uint8, tok [B*L] int32 (updated in
+    place at committed rows). ``masked_out`` may be ``masked`` itself (in
+    place). Returns (tok, masked_out).
+    """
+    import torch
+    _check_commit_args(logits, masked, tok)
     h = h or handle(logits.device.index)
     if masked_out is None:
         masked_out = torch.empty_like(masked)
-    need = commit_workspace_bytes(B, L)
-    if workspace is None or workspace.numel() * workspace.element_size() < need:
-        # zero-filled: the per-block tickets must start at zero (calls keep them so)
-        workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=logits.device)
     _check(lib().tt_commit(h.ptr, _dev_ptr(logits), int(B), int(L), int(logits.shape[1]),
                            _dev_ptr(masked), int(k), _dev_ptr(tok), _dev_ptr(masked_out),
-                           _dev_ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream_ptr(logits, stream)), "tt_commit")
-    return tok, masked_out, workspace
+    return tok, masked_out
 
 
 def commit_threshold(logits, B: int, L: int, masked, gamma: float, steps_left: int, tok,
-                     masked_out=None, workspace=None, h: Handle | None = None, stream=None):
+                     masked_out=None, h: Handle | None = None, stream=None):
     """One threshold unmasking step (Algorithm 2): per block, every masked row
     whose confidence is above gamma, and at least ceil(#masked / steps_left).
 
     Arguments and results as :func:`commit`.
     """
     import torch
-    if logits.dtype != torch.float32 or not logits.is_cuda or not logits.is_contiguous():
-        raise ValueError("logits must be a contiguous CUDA float32 tensor")
-    if masked.dtype != torch.uint8 or tok.dtype != torch.int32:
-        raise ValueError("masked must be uint8 and tok int32")
+    _check_commit_args(logits, masked, tok)
     h = h or handle(logits.device.index)
     if masked_out is None:
         masked_out = torch.empty_like(masked)
-    need = commit_workspace_bytes(B, L)
-    if workspace is None or workspace.numel() * workspace.element_size() < need:
-        workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=logits.device)
     _check(lib().tt_commit_threshold(h.ptr, _dev_ptr(logits), int(B), int(L), int(logits.shape[1]),
                                      _dev_ptr(masked), float(gamma), int(steps_left), _dev_ptr(tok),
-                                     _dev_ptr(masked_out), _dev_ptr(workspace),
-                                     workspace.numel() * workspace.element_size(),
-                                     _stream_ptr(logits, stream)), "tt_commit_threshold")
-    return tok, masked_out, workspace
+                                     _dev_ptr(masked_out), _stream_ptr(logits, stream)),
+           "tt_commit_threshold")
+    return tok, masked_out
 
 
-def commit_keys(workspace, B: int, L: int):
-    """Views of (key[B*L] as int64 bits, arg[B*L]) inside a commit workspace."""
+def commit_keys(rows: int, h: Handle | None = None, device=None, stream=None):
+    """(key[rows] as int64 bits, arg[rows] int32) of the last commit call on the
+    handle (tt_commit_keys), as new device tensors."""
     import torch
-    rows = B * L
-    off = (rows * 8 + 255) // 256 * 256
-    keys = workspace[:rows * 8].view(torch.int64)
-    args = workspace[off:off + rows * 4].view(torch.int32)
+    h = h or handle(device)
+    dev = torch.device("cuda", h.device)
+    keys = torch.empty(rows, dtype=torch.int64, device=dev)
+    args = torch.empty(rows, dtype=torch.int32, device=dev)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    _check(lib().tt_commit_keys(h.ptr, _dev_ptr(keys), _dev_ptr(args), int(rows),
+                                ctypes.c_void_p(st.cuda_stream)), "tt_commit_keys")
     return keys, args

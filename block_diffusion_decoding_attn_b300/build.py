@@ -10,7 +10,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libtt.so")
-SOURCES = ["tt_api.cu", "block_attn.cu", "commit.cu", "commit_noalloc.cu", "kv_append.cu"]
+SOURCES = ["tt_api.cu", "block_attn.cu", "block_attn_split.cu", "commit.cu", "commit_noalloc.cu",
+           "kv_append.cu"]
 HEADERS = ["ptx.cuh", "tt_internal.h"]
 
 NVCC_FLAGS = [

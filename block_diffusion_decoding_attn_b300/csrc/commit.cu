@@ -420,6 +420,21 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* a, unsigned v
     return old;
 }
 
+__device__ __forceinline__ void red_add_release_gpu(unsigned* a, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* a) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+// Counters of one call (zero between calls).
+constexpr int kCtrStarted = 0;   // clusters past their start-up mask scan
+constexpr int kCtrFinished = 1;  // clusters done
+constexpr int kCtrTickets = 2;   // block b's ticket at kCtrTickets + b
+
 // Masked rows of block b (read by one warp).
 __device__ int count_masked(const CommitParams& p, int b, int lane) {
     const uint8_t* m = p.masked + static_cast<size_t>(b) * p.L;
@@ -524,6 +539,10 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
     // Every CTA's barriers are initialised before any remote arrival.
     cluster_sync_all();
     tc_fence_after();
+    // The cluster's scans are over. When masked_out is the masked buffer, no
+    // block selection writes the mask before every cluster has scanned it (the
+    // selecting warp waits for this count to reach the number of clusters).
+    if (rank == 0 && tid == 0) red_add_release_gpu(p.counters + kCtrStarted, 1u);
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------------- producer
@@ -588,10 +607,23 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 if (lane == 0) {
                     // acq_rel: the rows' key / arg are visible before the ticket;
                     // the last ticket sees every other cluster's rows.
-                    const unsigned t = atom_add_acq_rel_gpu(p.counters + cb, static_cast<unsigned>(cmine));
+                    unsigned* tk = p.counters + kCtrTickets + cb;
+                    const unsigned t = atom_add_acq_rel_gpu(tk, static_cast<unsigned>(cmine));
                     last = t + static_cast<unsigned>(cmine) == static_cast<unsigned>(cnum);
-                    if (last) p.counters[cb] = 0;  // no other ticket of this call remains
+                    if (last) *tk = 0;  // no other ticket of this call remains
+                    if (last && p.alias) {
+                        // the mask is written in place: every cluster has scanned it first
+                        const uint64_t t0 = globaltimer_ns();
+                        while (ld_acquire_gpu(p.counters + kCtrStarted) < static_cast<unsigned>(ncl)) {
+                            if (globaltimer_ns() - t0 > limit) {
+                                last = 0;
+                                ok = false;
+                                break;
+                            }
+                        }
+                    }
                 }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (__shfl_sync(0xffffffffu, last, 0)) {
                     __threadfence();  // every lane reads the other clusters' rows after the ticket
                     if (p.L <= 32 * kSelRegRows) select_block_small(p, cb, cnum, lane);
@@ -622,6 +654,7 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 const int b = r / p.L;
                 if (b != cb) {
                     if (cb >= 0) flush();
+                    if (!ok) break;
                     cb = b;
                     cmine = 0;
                     cnum = count_masked(p, b, lane);
@@ -849,6 +882,14 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
     // No CTA leaves while another may still write into its shared memory.
     tc_fence_before();
     cluster_sync_all();
+    // The last cluster to finish puts the call's counters back to zero.
+    if (rank == 0 && tid == 0) {
+        const unsigned f = atom_add_acq_rel_gpu(p.counters + kCtrFinished, 1u);
+        if (f + 1 == static_cast<unsigned>(ncl)) {
+            p.counters[kCtrStarted] = 0;
+            p.counters[kCtrFinished] = 0;
+        }
+    }
     // A receiver that gave up may still be the target of a message issued
     // before its sender reached the barrier above: give it 100 us to land
     // before this CTA's shared memory goes away (only after a timeout).

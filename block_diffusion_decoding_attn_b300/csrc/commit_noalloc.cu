@@ -6,7 +6,7 @@
 // point keeps the commit step's scratch (per-row keys and predictions,
 // per-block tickets) in a fixed array compiled into the library instead.
 //
-// The array holds kScratchBytes (1 MiB + 256 bytes) on every GPU that loads
+// The array holds kScratchBytes (about 1 MiB) on every GPU that loads
 // the library, until the process exits; it bounds B*L to 65536 rows. Every
 // call uses the same array, so calls whose work overlaps on the GPU (other
 // streams, other host threads) race on it and must be ordered by the caller.
@@ -21,8 +21,9 @@ constexpr int kMaxRows = 65536;    // B * L
 constexpr int kMaxBlocks = 65536;  // B
 constexpr size_t kKeyOff = 0;                                                    // uint64 key[kMaxRows]
 constexpr size_t kArgOff = kKeyOff + static_cast<size_t>(kMaxRows) * 8;          // int32 arg[kMaxRows]
-constexpr size_t kTicketOff = kArgOff + static_cast<size_t>(kMaxRows) * 4;       // uint32 ticket[kMaxBlocks]
-constexpr size_t kStatusOff = kTicketOff + static_cast<size_t>(kMaxBlocks) * 4;  // uint32 status
+// uint32 counters[2 + kMaxBlocks]: two per-call counters, then the block tickets
+constexpr size_t kTicketOff = kArgOff + static_cast<size_t>(kMaxRows) * 4;
+constexpr size_t kStatusOff = kTicketOff + static_cast<size_t>(2 + kMaxBlocks) * 4;  // uint32 status
 constexpr size_t kScratchBytes = kStatusOff + 256;
 
 // In host code this name is only a stand-in for the device array, not its
@@ -55,6 +56,10 @@ extern "C" int tt_commit_noalloc(const float* logits, int B, int L, int V, const
         return fail(TT_ERR_INVALID_ARG, "a tensor pointer is NULL");
     if ((reinterpret_cast<uintptr_t>(logits) & 15u) || (reinterpret_cast<uintptr_t>(tok) & 15u))
         return fail(TT_ERR_INVALID_ARG, "logits and tok must be 16-byte aligned");
+    const uintptr_t mi = reinterpret_cast<uintptr_t>(masked), mo = reinterpret_cast<uintptr_t>(masked_out);
+    const size_t rows = static_cast<size_t>(B) * L;
+    if (mi != mo && mi < mo + rows && mo < mi + rows)
+        return fail(TT_ERR_INVALID_ARG, "masked and masked_out overlap without being the same buffer");
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -75,11 +80,11 @@ extern "C" int tt_commit_noalloc(const float* logits, int B, int L, int V, const
         base = g_scratch_dev[dev];
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents. The block tickets must
-    // start at zero (a call that gave up on a wait may have left them
-    // otherwise), so they are cleared; the keys and predictions are written
-    // before they are read.
-    if (cudaMemsetAsync(base + kTicketOff, 0, static_cast<size_t>(B) * 4, s) != cudaSuccess)
+    // The array keeps the previous call's contents. The counters and block
+    // tickets must start at zero (a call that gave up on a wait may have left
+    // them otherwise), so they are cleared; the keys and predictions are
+    // written before they are read.
+    if (cudaMemsetAsync(base + kTicketOff, 0, static_cast<size_t>(2 + B) * 4, s) != cudaSuccess)
         return fail(TT_ERR_CUDA, "clearing the block tickets failed");
     tt::CommitParams p;
     p.logits = logits;
@@ -96,8 +101,30 @@ extern "C" int tt_commit_noalloc(const float* logits, int B, int L, int V, const
     p.key = reinterpret_cast<unsigned long long*>(base + kKeyOff);
     p.arg = reinterpret_cast<int32_t*>(base + kArgOff);
     p.counters = reinterpret_cast<unsigned*>(base + kTicketOff);
+    p.alias = mi == mo;
     p.status = reinterpret_cast<unsigned*>(base + kStatusOff);
     p.timeout_ns = 1000000000ull;
     if (tt::launch_commit(p, s) != cudaSuccess) return fail(TT_ERR_CUDA, "commit launch failed");
     return TT_OK;
+}
+
+extern "C" int tt_commit_noalloc_status(int* device_status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail(TT_ERR_CUDA, "no usable current CUDA device");
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        if (!g_scratch_dev[dev])
+            return fail(TT_ERR_INVALID_ARG, "no tt_commit_noalloc call was made on this device");
+    }
+    unsigned v = 0;
+    const unsigned zero = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return fail(TT_ERR_CUDA, "cudaDeviceSynchronize failed");
+    // Synchronous copies of the status word inside the built-in array.
+    if (cudaMemcpyFromSymbol(&v, g_commit_scratch, sizeof v, kStatusOff) != cudaSuccess)
+        return fail(TT_ERR_CUDA, "reading the status word failed");
+    if (cudaMemcpyToSymbol(g_commit_scratch, &zero, sizeof zero, kStatusOff) != cudaSuccess)
+        return fail(TT_ERR_CUDA, "clearing the status word failed");
+    if (device_status) *device_status = static_cast<int>(v);
+    return (v & tt::kDevWaitTimeout) ? TT_ERR_TIMEOUT : TT_OK;
 }

@@ -17,6 +17,29 @@ struct tt_context {
     int num_sms;
     unsigned* status;  // device word, TT_DEV_* bits
     unsigned long long timeout_ns;
+    // Workspace owned by the handle: attention partials or commit keys and
+    // predictions (calls on one handle are ordered on the GPU, so they share
+    // it), and counters that every kernel leaves at zero.
+    void* ws;
+    size_t ws_bytes;
+    unsigned* ctr;
+    size_t ctr_count;
+    int attn_kernel;  // attention schedule: 0 by shape, 1 one unit per CTA, 2 persistent
+    int max_ctas;     // persistent schedule: CTAs at most (0: one per SM)
+    int min_tiles;    // persistent schedule: KV tiles per group at least
+    int splits;       // one-unit-per-CTA schedule: KV splits per unit (0: by shape)
+    // Encoded TMA descriptors of recent calls (encoding one costs microseconds
+    // of host time; a caller that reuses its buffers hits this cache).
+    struct MapEntry {
+        void* base;
+        int rank;
+        cuuint64_t dims[5], strides[4];
+        cuuint32_t box[5];
+        unsigned long long used;
+        CUtensorMap map;
+    };
+    MapEntry maps[32];
+    unsigned long long map_clock;
 };
 
 namespace {
@@ -74,16 +97,27 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+
 struct AttnPlan {
-    int G, n_mtiles, n_pairs, nblk, nt_max, splits, chunk;
-    size_t ws_o_bytes, ws_bytes;
+    int G, n_mtiles, n_pairs, nblk, width, ngroups;
+    size_t part_o_bytes, ws_bytes, ctr_count;
 };
 
-// Checks a descriptor; fills the launch plan. Split choice: minimise
-// waves * (tiles per split + 2) over the split count, where one wave is one
-// CTA per SM (the kernel's shared memory allows one) and the +2 stands for the
-// per-CTA prologue and epilogue; a split sequence also pays for the merge.
-int plan_attn(const tt_attn_desc* d, int num_sms, AttnPlan* pl) {
+// Largest divisor of n that is <= cap.
+int divisor_at_most(int n, int cap) {
+    for (int w = cap < n ? cap : n; w > 1; --w)
+        if (n % w == 0) return w;
+    return 1;
+}
+
+// Checks a descriptor; fills the launch plan. `cache_seqs` = sequences of the
+// context cache (B, or fewer in the training layout). Schedule: one CTA per SM
+// (at most max_ctas), in groups of `width` CTAs that take the pairs of a pair
+// block together. The width is a divisor of the pair count: up to 4 when the
+// whole cache fits comfortably in L2 (any order then reads it once from HBM),
+// up to 16 otherwise, so that the pairs reading one K/V tile run at the same
+// time.
+int plan_attn(const tt_attn_desc* d, int num_sms, int max_ctas, int cache_seqs, AttnPlan* pl) {
     if (!d) return fail(TT_ERR_INVALID_ARG, "tt_block_attn: desc is NULL");
     if (d->B < 0 || d->B > 65535) return fail(TT_ERR_INVALID_ARG, "B=%d outside [0, 65535]", d->B);
     if (d->L < 1 || d->L > 65536) return fail(TT_ERR_INVALID_ARG, "L=%d outside [1, 65536]", d->L);
@@ -98,40 +132,132 @@ int plan_attn(const tt_attn_desc* d, int num_sms, AttnPlan* pl) {
         return fail(TT_ERR_INVALID_ARG, "ctx_cap=%d outside [0, 2^24]", d->ctx_cap);
     if (!(d->scale >= 0.f) || std::isinf(d->scale))
         return fail(TT_ERR_INVALID_ARG, "scale must be finite and >= 0");
-    if (d->num_splits < 0) return fail(TT_ERR_INVALID_ARG, "num_splits must be >= 0");
     pl->G = G;
     pl->n_mtiles = static_cast<int>((static_cast<long>(G) * d->L + tt::kTile - 1) / tt::kTile);
     pl->n_pairs = (pl->n_mtiles + 1) / 2;
     pl->nblk = (d->L + tt::kTile - 1) / tt::kTile;
-    pl->nt_max = (d->ctx_cap + tt::kTile - 1) / tt::kTile + pl->nblk;
-    const long units = static_cast<long>(d->B) * d->Hkv * pl->n_pairs;
+    const double kv_bytes = 4.0 * cache_seqs * d->Hkv * static_cast<double>(d->ctx_cap) * d->D;
+    pl->width = divisor_at_most(pl->n_pairs, kv_bytes > 48e6 ? 16 : 4);
+    int ctas = num_sms;
+    if (max_ctas > 0 && max_ctas < ctas) ctas = max_ctas;
+    pl->ngroups = ctas / pl->width > 0 ? ctas / pl->width : 1;
+    const size_t slots = 2 * static_cast<size_t>(pl->ngroups) * pl->width;
+    pl->part_o_bytes = align256(slots * tt::attn_slot_o_floats(d->D) * sizeof(float));
+    pl->ws_bytes = pl->part_o_bytes + align256(slots * tt::attn_slot_ml(d->D) * sizeof(float2));
+    pl->ctr_count = static_cast<size_t>(d->B) * d->Hkv * pl->n_mtiles;
+    return TT_OK;
+}
+
+// The one-unit-per-CTA schedule's KV split: the split count minimising
+// waves * (tiles per split + 2) over the capacity's tiles (one CTA per SM; the
+// +2 stands for a CTA's prologue and epilogue; a split also pays for the
+// merge), or `forced` splits. Fills splits, chunk and the partials' bytes.
+struct SplitPlan {
+    int splits, chunk;
+    size_t ws_o_bytes, ws_bytes;
+};
+
+SplitPlan plan_split(const tt_attn_desc* d, const AttnPlan& pl, int num_sms, int forced) {
+    SplitPlan sp;
+    const int nt_max = (d->ctx_cap + tt::kTile - 1) / tt::kTile + pl.nblk;
+    const long units = static_cast<long>(d->B) * d->Hkv * pl.n_pairs;
     int best = 1;
-    if (d->num_splits > 0) {
-        best = d->num_splits < pl->nt_max ? d->num_splits : pl->nt_max;
+    if (forced > 0) {
+        best = forced < nt_max ? forced : nt_max;
     } else if (units > 0) {
         double best_cost = 1e300;
-        const int smax = pl->nt_max < 64 ? pl->nt_max : 64;
+        const int smax = nt_max < 64 ? nt_max : 64;
         for (int s = 1; s <= smax; ++s) {
-            const int chunk = (pl->nt_max + s - 1) / s;
-            const int s2 = (pl->nt_max + chunk - 1) / chunk;
+            const int chunk = (nt_max + s - 1) / s;
+            const int s2 = (nt_max + chunk - 1) / chunk;
             if (s2 != s) continue;
             const long waves = (units * s2 + num_sms - 1) / num_sms;
             const double cost = static_cast<double>(waves) * (chunk + 2) + (s2 > 1 ? 2 : 0);
             if (cost < best_cost) { best_cost = cost; best = s2; }
         }
     }
-    pl->chunk = (pl->nt_max + best - 1) / best;
-    pl->splits = (pl->nt_max + pl->chunk - 1) / pl->chunk;
-    if (pl->splits > 1) {
-        const size_t rows = static_cast<size_t>(pl->splits) * d->B * d->Hkv *
-                            static_cast<size_t>(pl->n_mtiles) * tt::kTile;
-        pl->ws_o_bytes = align256(rows * d->D * sizeof(float));
-        pl->ws_bytes = pl->ws_o_bytes + align256(rows * 2 * sizeof(float));
+    sp.chunk = (nt_max + best - 1) / best;
+    sp.splits = (nt_max + sp.chunk - 1) / sp.chunk;
+    if (sp.splits > 1) {
+        const size_t rows = static_cast<size_t>(sp.splits) * d->B * d->Hkv *
+                            static_cast<size_t>(pl.n_mtiles) * tt::kTile;
+        sp.ws_o_bytes = align256(rows * d->D * sizeof(float));
+        sp.ws_bytes = sp.ws_o_bytes + align256(rows * 2 * sizeof(float));
     } else {
-        pl->ws_o_bytes = pl->ws_bytes = 0;
+        sp.ws_o_bytes = sp.ws_bytes = 0;
     }
-    const long grid_x = static_cast<long>(pl->n_pairs) * pl->splits;
-    if (grid_x > 0x7fffffffL) return fail(TT_ERR_UNSUPPORTED, "grid too large");
+    return sp;
+}
+
+// Which attention schedule a call takes: the persistent stream-K kernel for
+// long caches (its per-range cost is small against long units, and it
+// balances ragged lengths), one unit per CTA otherwise (faster per tile on
+// short or equal-length units, and for the training layout's many short
+// units).
+bool use_persistent(const tt_context* h, const tt_attn_desc* d, int ctx_group) {
+    if (h->attn_kernel == 1) return false;
+    if (h->attn_kernel == 2) return true;
+    return !ctx_group && d->ctx_cap >= 16384;
+}
+
+size_t commit_ws_bytes(size_t rows) { return align256(rows * 8) + align256(rows * 4); }
+
+// Grows the handle's workspace and counters to at least the given sizes. A
+// growth synchronizes the device (the old buffers may still be in use) and
+// allocates; the new counters are zeroed.
+int ensure_workspace(tt_context* h, size_t ws_bytes, size_t ctr_count) {
+    cudaError_t e;
+    if (ws_bytes > h->ws_bytes) {
+        const size_t n = (ws_bytes + (1u << 20) - 1) & ~static_cast<size_t>((1u << 20) - 1);
+        if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        if (h->ws) cudaFree(h->ws);
+        h->ws = nullptr;
+        h->ws_bytes = 0;
+        if ((e = cudaMalloc(&h->ws, n)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+        h->ws_bytes = n;
+    }
+    if (ctr_count > h->ctr_count) {
+        const size_t n = (ctr_count + 4095) & ~static_cast<size_t>(4095);
+        if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        if (h->ctr) cudaFree(h->ctr);
+        h->ctr = nullptr;
+        h->ctr_count = 0;
+        if ((e = cudaMalloc(&h->ctr, n * sizeof(unsigned))) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(counters)");
+        if ((e = cudaMemset(h->ctr, 0, n * sizeof(unsigned))) != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(counters)");
+        h->ctr_count = n;
+    }
+    return TT_OK;
+}
+
+int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+           const cuuint32_t* box, const char* name);
+
+// encode() through the handle's descriptor cache (least recently used out).
+int encode_cached(tt_context* h, CUtensorMap* m, void* base, int rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box, const char* name) {
+    tt_context::MapEntry* victim = &h->maps[0];
+    for (auto& e : h->maps) {
+        if (e.used && e.base == base && e.rank == rank &&
+            !std::memcmp(e.dims, dims, sizeof(cuuint64_t) * rank) &&
+            !std::memcmp(e.strides, strides, sizeof(cuuint64_t) * (rank - 1)) &&
+            !std::memcmp(e.box, box, sizeof(cuuint32_t) * rank)) {
+            e.used = ++h->map_clock;
+            *m = e.map;
+            return TT_OK;
+        }
+        if (e.used < victim->used) victim = &e;
+    }
+    const int st = encode(m, base, rank, dims, strides, box, name);
+    if (st != TT_OK) return st;
+    victim->base = base;
+    victim->rank = rank;
+    std::memcpy(victim->dims, dims, sizeof(cuuint64_t) * rank);
+    std::memcpy(victim->strides, strides, sizeof(cuuint64_t) * (rank - 1));
+    std::memcpy(victim->box, box, sizeof(cuuint32_t) * rank);
+    victim->map = *m;
+    victim->used = ++h->map_clock;
     return TT_OK;
 }
 
@@ -147,6 +273,26 @@ int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const c
     return TT_OK;
 }
 
+// Checks a training-layout descriptor and gives the equivalent per-block one.
+int train_desc(const tt_train_desc* t, tt_attn_desc* d) {
+    if (!t) return fail(TT_ERR_INVALID_ARG, "tt_block_attn_train: desc is NULL");
+    if (t->B < 0) return fail(TT_ERR_INVALID_ARG, "B=%d < 0", t->B);
+    if (t->S < 1 || t->N < t->S || t->N % t->S)
+        return fail(TT_ERR_INVALID_ARG, "N=%d must be a positive multiple of the block size S=%d",
+                    t->N, t->S);
+    const long blocks = static_cast<long>(t->B) * (t->N / t->S);
+    if (blocks > 65535)
+        return fail(TT_ERR_UNSUPPORTED, "B * N / S = %ld noisy blocks (at most 65535)", blocks);
+    d->B = static_cast<int>(blocks);
+    d->L = t->S;
+    d->Hq = t->Hq;
+    d->Hkv = t->Hkv;
+    d->D = t->D;
+    d->ctx_cap = t->N;
+    d->scale = t->scale;
+    return TT_OK;
+}
+
 }  // namespace
 
 void tt::record_host_error(const char* where, const char* msg) { fail(0, "%s: %s", where, msg); }
@@ -159,8 +305,8 @@ const char* tt_status_string(int s) {
         case TT_ERR_INVALID_ARG: return "TT_ERR_INVALID_ARG";
         case TT_ERR_UNSUPPORTED: return "TT_ERR_UNSUPPORTED";
         case TT_ERR_CUDA: return "TT_ERR_CUDA";
-        case TT_ERR_DEVICE: return "TT_ERR_DEVICE";
-        case TT_ERR_WORKSPACE: return "TT_ERR_WORKSPACE";
+        case TT_ERR_TIMEOUT: return "TT_ERR_TIMEOUT";
+        case TT_ERR_DEVICE_CHECK: return "TT_ERR_DEVICE_CHECK";
         default: return "TT_ERR_UNKNOWN";
     }
 }
@@ -183,11 +329,14 @@ int tt_create(tt_handle* out, int device) {
         return fail(TT_ERR_CUDA, "device %d is sm_%d%d; this library is built for sm_103a", device,
                     prop.major, prop.minor);
     if ((e = tt::configure_attn_kernels()) != cudaSuccess) return cuda_fail(e, "attention kernel attributes");
+    if ((e = tt::configure_attn_split_kernels()) != cudaSuccess)
+        return cuda_fail(e, "attention kernel attributes");
     if ((e = tt::configure_commit_kernels()) != cudaSuccess) return cuda_fail(e, "commit kernel attributes");
     tt_context* h = new tt_context();
     h->device = device;
     h->num_sms = prop.multiProcessorCount;
     h->timeout_ns = 1000000000ull;
+    h->min_tiles = 8;
     if ((e = cudaMalloc(&h->status, sizeof(unsigned))) != cudaSuccess) {
         delete h;
         return cuda_fail(e, "cudaMalloc(status)");
@@ -197,6 +346,16 @@ int tt_create(tt_handle* out, int device) {
         delete h;
         return cuda_fail(e, "cudaMemset(status)");
     }
+    // The attention partials of a full grid at D = 128 and 64 Ki counters up
+    // front, so that the usual shapes never allocate on the call path.
+    const size_t slots = 2 * static_cast<size_t>(h->num_sms);
+    const size_t ws0 = align256(slots * tt::attn_slot_o_floats(128) * sizeof(float)) +
+                       align256(slots * tt::attn_slot_ml(128) * sizeof(float2));
+    const int st = ensure_workspace(h, ws0, 65536);
+    if (st != TT_OK) {
+        tt_destroy(h);
+        return st;
+    }
     *out = h;
     return TT_OK;
 }
@@ -205,6 +364,8 @@ int tt_destroy(tt_handle h) {
     if (!h) return TT_OK;
     DeviceGuard g(h->device);
     cudaFree(h->status);
+    if (h->ws) cudaFree(h->ws);
+    if (h->ctr) cudaFree(h->ctr);
     delete h;
     return TT_OK;
 }
@@ -216,7 +377,39 @@ int tt_set_wait_timeout(tt_handle h, unsigned long long ns) {
     return TT_OK;
 }
 
-int tt_get_error(tt_handle h, unsigned* device_status) {
+int tt_set_attn_schedule(tt_handle h, int kernel, int max_ctas, int min_tiles, int splits) {
+    if (!h) return fail(TT_ERR_INVALID_ARG, "handle is NULL");
+    if (kernel < 0 || kernel > 2) return fail(TT_ERR_INVALID_ARG, "kernel must be 0, 1 or 2");
+    if (max_ctas < 0 || min_tiles < 0 || splits < 0)
+        return fail(TT_ERR_INVALID_ARG, "max_ctas, min_tiles and splits must be >= 0");
+    h->attn_kernel = kernel;
+    h->max_ctas = max_ctas;
+    h->min_tiles = min_tiles > 0 ? min_tiles : 8;
+    h->splits = splits;
+    return TT_OK;
+}
+
+int tt_reserve(tt_handle h, const tt_attn_desc* attn, int commit_B, int commit_L) {
+    if (!h) return fail(TT_ERR_INVALID_ARG, "tt_reserve: handle is NULL");
+    if (commit_B < 0 || commit_L < 0) return fail(TT_ERR_INVALID_ARG, "tt_reserve: negative size");
+    DeviceGuard g(h->device);
+    if (!g.ok()) return fail(TT_ERR_CUDA, "cannot select device %d", h->device);
+    size_t ws = 0, ctr = 0;
+    if (attn) {
+        AttnPlan pl;
+        const int st = plan_attn(attn, h->num_sms, h->max_ctas, attn->B, &pl);
+        if (st != TT_OK) return st;
+        const SplitPlan sp = plan_split(attn, pl, h->num_sms, h->splits);
+        ws = pl.ws_bytes > sp.ws_bytes ? pl.ws_bytes : sp.ws_bytes;
+        ctr = pl.ctr_count;
+    }
+    const size_t rows = static_cast<size_t>(commit_B) * commit_L;
+    if (commit_ws_bytes(rows) > ws) ws = commit_ws_bytes(rows);
+    if (2 + static_cast<size_t>(commit_B) > ctr) ctr = 2 + static_cast<size_t>(commit_B);
+    return ensure_workspace(h, ws, ctr);
+}
+
+int tt_get_error(tt_handle h, int* device_status) {
     if (!h) return fail(TT_ERR_INVALID_ARG, "handle is NULL");
     DeviceGuard g(h->device);
     cudaError_t e = cudaDeviceSynchronize();
@@ -225,16 +418,16 @@ int tt_get_error(tt_handle h, unsigned* device_status) {
     if ((e = cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
         return cuda_fail(e, "read status");
     if ((e = cudaMemset(h->status, 0, sizeof v)) != cudaSuccess) return cuda_fail(e, "clear status");
-    if (device_status) *device_status = v;
-    return v ? TT_ERR_DEVICE : TT_OK;
+    // A call that gave up on a wait may have left tickets behind.
+    if ((v & TT_DEV_WAIT_TIMEOUT) && h->ctr &&
+        (e = cudaMemset(h->ctr, 0, h->ctr_count * sizeof(unsigned))) != cudaSuccess)
+        return cuda_fail(e, "clear counters");
+    if (device_status) *device_status = static_cast<int>(v);
+    if (v & TT_DEV_WAIT_TIMEOUT) return TT_ERR_TIMEOUT;
+    return v ? TT_ERR_DEVICE_CHECK : TT_OK;
 }
 
-size_t tt_block_attn_workspace_bytes(tt_handle h, const tt_attn_desc* d) {
-    if (!h) return 0;
-    AttnPlan pl;
-    if (plan_attn(d, h->num_sms, &pl) != TT_OK) return 0;
-    return pl.ws_bytes;
-}
+}  // extern "C"
 
 // Body of tt_block_attn (causal = 0), tt_block_attn_causal (causal = 1) and
 // tt_block_attn_train (ctx_group = blocks per clean sequence: d->B counts the
@@ -242,11 +435,12 @@ size_t tt_block_attn_workspace_bytes(tt_handle h, const tt_attn_desc* d) {
 // ctx_len is implied).
 static int block_attn_call(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
                            const void* v_blk, const void* k_ctx, const void* v_ctx,
-                           const int32_t* ctx_len, void* out, void* workspace,
-                           size_t workspace_bytes, void* stream, int causal, int ctx_group = 0) {
+                           const int32_t* ctx_len, void* out, void* stream, int causal,
+                           int ctx_group = 0) {
     if (!h) return fail(TT_ERR_INVALID_ARG, "tt_block_attn: handle is NULL");
     AttnPlan pl;
-    int st = plan_attn(d, h->num_sms, &pl);
+    const int cache_seqs = d && ctx_group ? d->B / ctx_group : (d ? d->B : 0);
+    int st = plan_attn(d, h->num_sms, h->max_ctas, cache_seqs, &pl);
     if (st != TT_OK) return st;
     if (d->B == 0) return TT_OK;
     if (!q || !k_blk || !v_blk || (!ctx_len && !ctx_group) || !out)
@@ -256,12 +450,15 @@ static int block_attn_call(tt_handle h, const tt_attn_desc* d, const void* q, co
     if (!aligned16(q) || !aligned16(k_blk) || !aligned16(v_blk) || !aligned16(out) ||
         (d->ctx_cap > 0 && (!aligned16(k_ctx) || !aligned16(v_ctx))))
         return fail(TT_ERR_INVALID_ARG, "tt_block_attn: tensors must be 16-byte aligned");
-    if (pl.ws_bytes > 0 && (!workspace || workspace_bytes < pl.ws_bytes ||
-                            (reinterpret_cast<uintptr_t>(workspace) & 255u)))
-        return fail(TT_ERR_WORKSPACE, "tt_block_attn: needs %zu workspace bytes (256-byte aligned)",
-                    pl.ws_bytes);
+    if (ctx_len && (reinterpret_cast<uintptr_t>(ctx_len) & 3u))
+        return fail(TT_ERR_INVALID_ARG, "tt_block_attn: ctx_len must be 4-byte aligned");
     DeviceGuard g(h->device);
     if (!g.ok()) return fail(TT_ERR_CUDA, "cannot select device %d", h->device);
+    const bool persistent = use_persistent(h, d, ctx_group);
+    const SplitPlan sp = persistent ? SplitPlan{1, 0, 0, 0} : plan_split(d, pl, h->num_sms, h->splits);
+    if ((st = ensure_workspace(h, persistent ? pl.ws_bytes : sp.ws_bytes, persistent ? pl.ctr_count : 0)) !=
+        TT_OK)
+        return st;
 
     const int B = d->B, L = d->L, Hq = d->Hq, Hkv = d->Hkv, D = d->D, G = pl.G;
     const cuuint64_t e2 = 2;  // bytes per bf16
@@ -272,15 +469,15 @@ static int block_attn_call(tt_handle h, const tt_attn_desc* d, const void* q, co
         const cuuint64_t str[4] = {D * e2, (cuuint64_t)G * D * e2, (cuuint64_t)Hq * D * e2,
                                    (cuuint64_t)L * Hq * D * e2};
         const cuuint32_t box[5] = {64, (cuuint32_t)G, 1, (cuuint32_t)(tt::kTile / G), 1};
-        if ((st = encode(&maps.q, const_cast<void*>(q), 5, dims, str, box, "q")) != TT_OK) return st;
+        if ((st = encode_cached(h, &maps.q, const_cast<void*>(q), 5, dims, str, box, "q")) != TT_OK) return st;
     }
     {
         const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)L, (cuuint64_t)B};
         const cuuint64_t str[3] = {D * e2, (cuuint64_t)Hkv * D * e2, (cuuint64_t)L * Hkv * D * e2};
         const cuuint32_t box[4] = {64, 1, (cuuint32_t)tt::kTile, 1};
-        if ((st = encode(&maps.k_blk, const_cast<void*>(k_blk), 4, dims, str, box, "k_blk")) != TT_OK)
+        if ((st = encode_cached(h, &maps.k_blk, const_cast<void*>(k_blk), 4, dims, str, box, "k_blk")) != TT_OK)
             return st;
-        if ((st = encode(&maps.v_blk, const_cast<void*>(v_blk), 4, dims, str, box, "v_blk")) != TT_OK)
+        if ((st = encode_cached(h, &maps.v_blk, const_cast<void*>(v_blk), 4, dims, str, box, "v_blk")) != TT_OK)
             return st;
     }
     {
@@ -288,93 +485,87 @@ static int block_attn_call(tt_handle h, const tt_attn_desc* d, const void* q, co
         // only need to be well formed, so they point at the block keys.
         const bool none = d->ctx_cap == 0;
         const cuuint64_t dims[3] = {(cuuint64_t)D, none ? (cuuint64_t)tt::kTile : (cuuint64_t)d->ctx_cap,
-                                    none ? 1 : (cuuint64_t)(ctx_group ? B / ctx_group : B) * Hkv};
+                                    none ? 1 : (cuuint64_t)cache_seqs * Hkv};
         const cuuint64_t str[2] = {D * e2, (none ? (cuuint64_t)tt::kTile : (cuuint64_t)d->ctx_cap) * D * e2};
         const cuuint32_t box[3] = {64, (cuuint32_t)tt::kTile, 1};
         void* kc = none ? const_cast<void*>(k_blk) : const_cast<void*>(k_ctx);
         void* vc = none ? const_cast<void*>(v_blk) : const_cast<void*>(v_ctx);
-        if ((st = encode(&maps.k_ctx, kc, 3, dims, str, box, "k_ctx")) != TT_OK) return st;
-        if ((st = encode(&maps.v_ctx, vc, 3, dims, str, box, "v_ctx")) != TT_OK) return st;
+        if ((st = encode_cached(h, &maps.k_ctx, kc, 3, dims, str, box, "k_ctx")) != TT_OK) return st;
+        if ((st = encode_cached(h, &maps.v_ctx, vc, 3, dims, str, box, "v_ctx")) != TT_OK) return st;
+    }
+    const float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(D));
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (!persistent) {
+        tt::AttnSplitParams q;
+        q.B = B; q.L = L; q.Hq = Hq; q.Hkv = Hkv; q.G = G; q.ctx_cap = d->ctx_cap;
+        q.n_mtiles = pl.n_mtiles; q.n_pairs = pl.n_pairs; q.nblk = pl.nblk;
+        q.causal = causal;
+        q.ctx_group = ctx_group;
+        q.chunk = sp.chunk;
+        q.scale_log2 = scale * 1.4426950408889634f;
+        q.ctx_len = ctx_len;
+        q.out = static_cast<__nv_bfloat16*>(out);
+        q.ws_o = sp.splits > 1 ? static_cast<float*>(h->ws) : nullptr;
+        q.ws_ml = sp.splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(h->ws) + sp.ws_o_bytes)
+                                : nullptr;
+        q.status = h->status;
+        q.timeout_ns = h->timeout_ns;
+        cudaError_t e = tt::launch_block_attn_split(maps, q, D, sp.splits, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "block attention launch");
+        if (sp.splits > 1 && (e = tt::launch_attn_merge(q, D, cs)) != cudaSuccess)
+            return cuda_fail(e, "split merge launch");
+        return TT_OK;
     }
     tt::AttnParams p;
     p.B = B; p.L = L; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.ctx_cap = d->ctx_cap;
-    p.n_mtiles = pl.n_mtiles; p.n_pairs = pl.n_pairs; p.chunk = pl.chunk; p.nblk = pl.nblk;
+    p.n_mtiles = pl.n_mtiles; p.n_pairs = pl.n_pairs; p.nblk = pl.nblk;
     p.causal = causal;
     p.ctx_group = ctx_group;
-    const float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(D));
+    p.width = pl.width;
+    p.ngroups = pl.ngroups;
+    p.min_tiles = h->min_tiles;
+    // Measured fixed costs, in KV tiles' time: a unit's (Q load, pipeline
+    // start, epilogue) about 4 for short units; a cut's (partial out, ticket,
+    // merge) about 8. Every range stays longer than a unit's fixed cost.
+    p.item_cost = h->min_tiles > 4 ? 4 : h->min_tiles - 1;
+    p.cut_cost = 8;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.ctx_len = ctx_len;
     p.out = static_cast<__nv_bfloat16*>(out);
-    p.ws_o = pl.splits > 1 ? static_cast<float*>(workspace) : nullptr;
-    p.ws_ml = pl.splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.ws_o_bytes)
-                            : nullptr;
+    p.part_o = static_cast<float*>(h->ws);
+    p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(h->ws) + pl.part_o_bytes);
+    p.tickets = h->ctr;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = tt::launch_block_attn(maps, p, D, pl.splits, s);
+    const cudaError_t e = tt::launch_block_attn(maps, p, D, cs);
     if (e != cudaSuccess) return cuda_fail(e, "block attention launch");
-    if (pl.splits > 1) {
-        e = tt::launch_attn_merge(p, D, s);
-        if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
-    }
     return TT_OK;
 }
 
+extern "C" {
+
 int tt_block_attn(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
                   const void* v_blk, const void* k_ctx, const void* v_ctx,
-                  const int32_t* ctx_len, void* out, void* workspace, size_t workspace_bytes,
-                  void* stream) {
-    return block_attn_call(h, d, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out, workspace,
-                           workspace_bytes, stream, 0);
+                  const int32_t* ctx_len, void* out, void* stream) {
+    return block_attn_call(h, d, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out, stream, 0);
 }
 
 int tt_block_attn_causal(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
                          const void* v_blk, const void* k_ctx, const void* v_ctx,
-                         const int32_t* ctx_len, void* out, void* workspace,
-                         size_t workspace_bytes, void* stream) {
-    return block_attn_call(h, d, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out, workspace,
-                           workspace_bytes, stream, 1);
-}
-
-// Checks a training-layout descriptor and gives the equivalent per-block one.
-static int train_desc(const tt_train_desc* t, tt_attn_desc* d) {
-    if (!t) return fail(TT_ERR_INVALID_ARG, "tt_block_attn_train: desc is NULL");
-    if (t->B < 0) return fail(TT_ERR_INVALID_ARG, "B=%d < 0", t->B);
-    if (t->S < 1 || t->N < t->S || t->N % t->S)
-        return fail(TT_ERR_INVALID_ARG, "N=%d must be a positive multiple of the block size S=%d",
-                    t->N, t->S);
-    const long blocks = static_cast<long>(t->B) * (t->N / t->S);
-    if (blocks > 65535)
-        return fail(TT_ERR_UNSUPPORTED, "B * N / S = %ld noisy blocks (at most 65535)", blocks);
-    d->B = static_cast<int>(blocks);
-    d->L = t->S;
-    d->Hq = t->Hq;
-    d->Hkv = t->Hkv;
-    d->D = t->D;
-    d->ctx_cap = t->N;
-    d->scale = t->scale;
-    d->num_splits = t->num_splits;
-    return TT_OK;
-}
-
-size_t tt_block_attn_train_workspace_bytes(tt_handle h, const tt_train_desc* t) {
-    tt_attn_desc d;
-    if (!h || train_desc(t, &d) != TT_OK) return 0;
-    AttnPlan pl;
-    if (plan_attn(&d, h->num_sms, &pl) != TT_OK) return 0;
-    return pl.ws_bytes;
+                         const int32_t* ctx_len, void* out, void* stream) {
+    return block_attn_call(h, d, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out, stream, 1);
 }
 
 int tt_block_attn_train(tt_handle h, const tt_train_desc* t, const void* q, const void* k_noisy,
                         const void* v_noisy, const void* k_clean, const void* v_clean, void* out,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+                        void* stream) {
     if (!h) return fail(TT_ERR_INVALID_ARG, "tt_block_attn_train: handle is NULL");
     tt_attn_desc d;
     const int st = train_desc(t, &d);
     if (st != TT_OK) return st;
     if (t->B == 0) return TT_OK;
-    return block_attn_call(h, &d, q, k_noisy, v_noisy, k_clean, v_clean, nullptr, out, workspace,
-                           workspace_bytes, stream, 0, t->N / t->S);
+    return block_attn_call(h, &d, q, k_noisy, v_noisy, k_clean, v_clean, nullptr, out, stream, 0,
+                           t->N / t->S);
 }
 
 int tt_kv_append(tt_handle h, const tt_attn_desc* d, const void* k_blk, const void* v_blk,
@@ -410,10 +601,24 @@ int tt_kv_append(tt_handle h, const tt_attn_desc* d, const void* k_blk, const vo
     return TT_OK;
 }
 
-size_t tt_commit_workspace_bytes(int B, int L) {
-    if (B < 0 || L < 0) return 0;
-    const size_t rows = static_cast<size_t>(B) * L;
-    return align256(rows * 8) + align256(rows * 4) + static_cast<size_t>(B) * 4;
+int tt_commit_keys(tt_handle h, uint64_t* key_dst, int32_t* arg_dst, int rows, void* stream) {
+    if (!h) return fail(TT_ERR_INVALID_ARG, "tt_commit_keys: handle is NULL");
+    if (rows < 0) return fail(TT_ERR_INVALID_ARG, "tt_commit_keys: rows < 0");
+    const size_t n = static_cast<size_t>(rows);
+    if (commit_ws_bytes(n) > h->ws_bytes)
+        return fail(TT_ERR_INVALID_ARG, "tt_commit_keys: more rows than the last commit held");
+    if (n == 0) return TT_OK;
+    DeviceGuard g(h->device);
+    if (!g.ok()) return fail(TT_ERR_CUDA, "cannot select device %d", h->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (key_dst && (e = cudaMemcpyAsync(key_dst, h->ws, n * 8, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "tt_commit_keys: copy keys");
+    if (arg_dst &&
+        (e = cudaMemcpyAsync(arg_dst, static_cast<char*>(h->ws) + align256(n * 8), n * 4,
+                             cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "tt_commit_keys: copy predictions");
+    return TT_OK;
 }
 
 }  // extern "C"
@@ -441,8 +646,7 @@ unsigned long long key_threshold(double gamma) {
 
 int commit_impl(tt_handle h, const char* name, const float* logits, int B, int L, int V,
                 const uint8_t* masked, int k, int steps_left, unsigned long long kthr,
-                int32_t* tok, uint8_t* masked_out, void* workspace, size_t workspace_bytes,
-                void* stream) {
+                int32_t* tok, uint8_t* masked_out, void* stream) {
     if (!h) return fail(TT_ERR_INVALID_ARG, "%s: handle is NULL", name);
     if (B < 0) return fail(TT_ERR_INVALID_ARG, "%s: B=%d < 0", name, B);
     if (L < 1 || L > tt::kCommitMaxL)
@@ -457,11 +661,15 @@ int commit_impl(tt_handle h, const char* name, const float* logits, int B, int L
         return fail(TT_ERR_INVALID_ARG, "%s: a tensor pointer is NULL", name);
     if (!aligned16(logits)) return fail(TT_ERR_INVALID_ARG, "%s: logits must be 16-byte aligned", name);
     if (!aligned16(tok)) return fail(TT_ERR_INVALID_ARG, "%s: tok must be 16-byte aligned", name);
-    const size_t need = tt_commit_workspace_bytes(B, L);
-    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return fail(TT_ERR_WORKSPACE, "%s: needs %zu workspace bytes (256-byte aligned)", name, need);
+    const size_t rows = static_cast<size_t>(B) * L;
+    const uintptr_t mi = reinterpret_cast<uintptr_t>(masked), mo = reinterpret_cast<uintptr_t>(masked_out);
+    if (mi != mo && mi < mo + rows && mo < mi + rows)
+        return fail(TT_ERR_INVALID_ARG, "%s: masked and masked_out overlap without being the same buffer",
+                    name);
     DeviceGuard g(h->device);
     if (!g.ok()) return fail(TT_ERR_CUDA, "cannot select device %d", h->device);
+    int st = ensure_workspace(h, commit_ws_bytes(rows), 2 + static_cast<size_t>(B));
+    if (st != TT_OK) return st;
     tt::CommitParams p;
     p.logits = logits;
     p.B = B; p.L = L; p.V = V; p.k = k;
@@ -471,11 +679,10 @@ int commit_impl(tt_handle h, const char* name, const float* logits, int B, int L
     p.masked = masked;
     p.tok = tok;
     p.masked_out = masked_out;
-    p.key = static_cast<unsigned long long*>(workspace);
-    const size_t rows = static_cast<size_t>(B) * L;
-    p.arg = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + align256(rows * 8));
-    p.counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + align256(rows * 8) +
-                                             align256(rows * 4));
+    p.key = static_cast<unsigned long long*>(h->ws);
+    p.arg = reinterpret_cast<int32_t*>(static_cast<char*>(h->ws) + align256(rows * 8));
+    p.counters = h->ctr;
+    p.alias = mi == mo;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     cudaError_t e = tt::launch_commit(p, static_cast<cudaStream_t>(stream));
@@ -488,22 +695,19 @@ int commit_impl(tt_handle h, const char* name, const float* logits, int B, int L
 extern "C" {
 
 int tt_commit(tt_handle h, const float* logits, int B, int L, int V, const uint8_t* masked, int k,
-              int32_t* tok, uint8_t* masked_out, void* workspace, size_t workspace_bytes,
-              void* stream) {
+              int32_t* tok, uint8_t* masked_out, void* stream) {
     if (k < 1) return fail(TT_ERR_INVALID_ARG, "tt_commit: k=%d < 1", k);
-    return commit_impl(h, "tt_commit", logits, B, L, V, masked, k, 0, 0ull, tok, masked_out,
-                       workspace, workspace_bytes, stream);
+    return commit_impl(h, "tt_commit", logits, B, L, V, masked, k, 0, 0ull, tok, masked_out, stream);
 }
 
 int tt_commit_threshold(tt_handle h, const float* logits, int B, int L, int V,
                         const uint8_t* masked, double gamma, int steps_left, int32_t* tok,
-                        uint8_t* masked_out, void* workspace, size_t workspace_bytes,
-                        void* stream) {
+                        uint8_t* masked_out, void* stream) {
     if (steps_left < 1)
         return fail(TT_ERR_INVALID_ARG, "tt_commit_threshold: steps_left=%d < 1", steps_left);
     if (std::isnan(gamma)) return fail(TT_ERR_INVALID_ARG, "tt_commit_threshold: gamma is NaN");
     return commit_impl(h, "tt_commit_threshold", logits, B, L, V, masked, 1, steps_left,
-                       key_threshold(gamma), tok, masked_out, workspace, workspace_bytes, stream);
+                       key_threshold(gamma), tok, masked_out, stream);
 }
 
 }  // extern "C"

@@ -24,14 +24,45 @@ constexpr int kTile = 128;  // query rows per M tile and keys per KV tile
 struct AttnParams {
     int B, L, Hq, Hkv, G, ctx_cap;
     int n_mtiles;  // ceil(G*L / 128) query tiles per (b, kv head)
-    int n_pairs;   // ceil(n_mtiles / 2): a CTA takes two query tiles
-    int chunk;     // KV tiles per split
+    int n_pairs;   // ceil(n_mtiles / 2): a CTA takes two query tiles at a time
     int nblk;      // ceil(L / 128) tiles of block keys
     int causal;    // 1: block query l sees block keys 0..l only (context-tower update)
     // Batched training layout (0: off). Sequence b is noisy block b % ctx_group
     // of clean sequence b / ctx_group: it reads that sequence's cache, with
     // ctx_len = (b % ctx_group) * L (ctx_len is then not read).
     int ctx_group;
+    // Persistent schedule: the grid is `ngroups` groups of `width` CTAs. The
+    // n_pairs query-tile pairs of a (b, kv head) are cut into n_pairs / width
+    // pair blocks; a work unit of a group is (b, kv head, pair block) over the
+    // sequence's KV tiles, CTA j of the group taking pair j of the block. The
+    // units' KV tiles are laid end to end and cut into one contiguous range per
+    // group (at least min_tiles tiles each; groups past the work exit).
+    int width, ngroups, min_tiles;
+    int item_cost;  // line positions a unit takes beyond its tiles (< min_tiles)
+    int cut_cost;   // line positions a cut unit costs (partial out, ticket, merge)
+    float scale_log2;
+    const int32_t* ctx_len;
+    __nv_bfloat16* out;
+    // Partial results of a query tile whose KV tiles were cut between groups:
+    // two slots per CTA (its first and its last unit), each holding both query
+    // tiles: O as [2][D/4][128][4] fp32 and (running max, running sum) as
+    // [2][128] float2.
+    float* part_o;
+    float2* part_ml;
+    // One counter per query tile (B * Hkv * n_mtiles): the pieces of a cut
+    // tile take a ticket after writing their partial; the last one merges and
+    // puts the counter back to zero. Zero between calls.
+    unsigned* tickets;
+    unsigned* status;
+    unsigned long long timeout_ns;
+};
+
+// The one-unit-per-CTA schedule (block_attn_split.cu): one CTA per (b, KV
+// head, query-tile pair, KV split of `chunk` tiles).
+struct AttnSplitParams {
+    int B, L, Hq, Hkv, G, ctx_cap;
+    int n_mtiles, n_pairs, nblk, causal, ctx_group;
+    int chunk;     // KV tiles per split
     float scale_log2;
     const int32_t* ctx_len;
     __nv_bfloat16* out;
@@ -45,12 +76,15 @@ struct AttnMaps {
     CUtensorMap q, k_ctx, v_ctx, k_blk, v_blk;
 };
 
-// Bytes of dynamic shared memory the attention kernel needs for head dim D.
-int attn_smem_bytes(int D);
+// Partial-result bytes of one CTA slot for head dim D (both query tiles).
+constexpr size_t attn_slot_o_floats(int D) { return static_cast<size_t>(2) * kTile * D; }
+constexpr size_t attn_slot_ml(int /*D*/) { return static_cast<size_t>(2) * kTile; }
 
-cudaError_t launch_block_attn(const AttnMaps& maps, const AttnParams& p, int D, int splits,
-                              cudaStream_t s);
-cudaError_t launch_attn_merge(const AttnParams& p, int D, cudaStream_t s);
+cudaError_t launch_block_attn(const AttnMaps& maps, const AttnParams& p, int D, cudaStream_t s);
+cudaError_t launch_block_attn_split(const AttnMaps& maps, const AttnSplitParams& p, int D, int splits,
+                                    cudaStream_t s);
+cudaError_t launch_attn_merge(const AttnSplitParams& p, int D, cudaStream_t s);
+cudaError_t configure_attn_split_kernels();
 
 struct KvAppendParams {
     int B, L, Hkv, D, ctx_cap;
@@ -80,7 +114,10 @@ struct CommitParams {
     uint8_t* masked_out;
     unsigned long long* key;  // [B*L]
     int32_t* arg;             // [B*L]
-    unsigned* counters;       // [B] block tickets; zero between calls
+    // [2 + B], zero between calls: [0] clusters past their start-up mask
+    // scan, [1] clusters finished, [2 + b] block b's ticket.
+    unsigned* counters;
+    int alias;  // masked_out is the masked buffer: no mask write before every scan is done
     unsigned* status;
     unsigned long long timeout_ns;
 };

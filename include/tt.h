@@ -9,11 +9,17 @@
  *
  * Conventions (all entry points):
  *   - Plain C types only. Tensor arguments are DEVICE pointers to contiguous
- *     row-major arrays with the shapes given below; the caller owns every
- *     buffer, including the workspace. The library never allocates on the call
- *     path (only tt_create allocates: a 4-byte device status word).
+ *     row-major arrays with the shapes given below; the caller owns them.
+ *   - The handle owns the scratch the kernels need (attention partials, the
+ *     commit step's keys and predictions, and counters that every kernel
+ *     leaves at zero). tt_create sizes it for the usual shapes; a call with a
+ *     larger shape grows it first, which synchronizes the device and
+ *     allocates. tt_reserve does that growth up front (e.g. before capturing a
+ *     CUDA graph), after which no call of that size or smaller allocates.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
- *     stream). Calls are asynchronous on it.
+ *     stream). Calls are asynchronous on it. Calls on one handle share its
+ *     scratch, so their GPU work must be ordered (one stream, or events); use
+ *     one handle per stream for concurrent work.
  *   - Return value: TT_OK, or a negative tt_status for an error detected on
  *     the host before anything is launched (nothing is written then). The
  *     message of the last host error of the calling thread is available from
@@ -21,8 +27,7 @@
  *   - Errors detected on the device (a ctx_len outside [0, ctx_cap], a
  *     pipeline wait that timed out) set bits of the handle's status word; read
  *     and clear it with tt_get_error. Kernels never trap.
- *   - A handle may be used from one host thread at a time. Calls that share a
- *     workspace must be ordered on the GPU (same stream, or events).
+ *   - A handle may be used from one host thread at a time.
  */
 #ifndef TT_H_
 #define TT_H_
@@ -36,39 +41,66 @@ extern "C" {
 
 typedef enum {
     TT_OK = 0,
-    TT_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer       */
-    TT_ERR_UNSUPPORTED = -2, /* a shape outside the supported set (see below)    */
-    TT_ERR_CUDA = -3,        /* a CUDA runtime or driver call failed             */
-    TT_ERR_DEVICE = -4,      /* tt_get_error: the device status word is non-zero */
-    TT_ERR_WORKSPACE = -5    /* workspace pointer missing or too small           */
+    TT_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misaligned pointer             */
+    TT_ERR_UNSUPPORTED = -2,  /* a shape outside the supported set (see below)          */
+    TT_ERR_CUDA = -3,         /* a CUDA runtime or driver call failed                   */
+    TT_ERR_TIMEOUT = -4,      /* tt_get_error: a bounded wait in a kernel gave up       */
+    TT_ERR_DEVICE_CHECK = -5  /* tt_get_error: a kernel's argument check failed (ctx_len) */
 } tt_status;
 
 /* Bits of the device status word (tt_get_error). */
-#define TT_DEV_CTX_LEN_RANGE 1u /* a ctx_len[b] outside [0, ctx_cap] (it was clamped), or a block
-                                   that does not fit the cache (tt_kv_append skipped it) */
-#define TT_DEV_WAIT_TIMEOUT 2u  /* a bounded pipeline wait gave up; outputs invalid    */
+#define TT_DEV_CTX_LEN_RANGE 1 /* a ctx_len[b] outside [0, ctx_cap] (it was clamped), or a block
+                                  that does not fit the cache (tt_kv_append skipped it) */
+#define TT_DEV_WAIT_TIMEOUT 2  /* a bounded pipeline wait gave up; outputs invalid      */
 
 typedef struct tt_context* tt_handle;
 
+/* Shapes of one block-attention call (see the block attention section). */
+typedef struct tt_attn_desc_s {
+    int B, L, Hq, Hkv, D, ctx_cap;
+    float scale; /* softmax scale; 0 selects 1/sqrt(D) */
+} tt_attn_desc;
+
 /* Creates a handle bound to CUDA device `device` (made current while the
- * library works on it). Allocates the device status word and sets kernel
- * attributes. Returns TT_OK, TT_ERR_INVALID_ARG (handle NULL) or TT_ERR_CUDA
- * (no such device, or it is not a compute capability 10.3 part). */
+ * library works on it). Allocates the device status word and the scratch for
+ * the usual shapes (about 40 MB), and sets kernel attributes. Returns TT_OK,
+ * TT_ERR_INVALID_ARG (handle NULL) or TT_ERR_CUDA (no such device, it is not
+ * a compute capability 10.3 part, or an allocation failed). */
 int tt_create(tt_handle* handle, int device);
 
-/* Frees the handle. Synchronizes nothing: the caller makes sure no launch on
- * the handle is still running. NULL is a no-op. */
+/* Frees the handle and its scratch. Synchronizes nothing: the caller makes
+ * sure no launch on the handle is still running. NULL is a no-op. */
 int tt_destroy(tt_handle handle);
+
+/* Grows the handle's scratch so that tt_block_attn / tt_block_attn_causal /
+ * tt_kv_append with descriptor `attn` (may be NULL) and tt_commit /
+ * tt_commit_threshold with B = commit_B, L = commit_L (0 for none) allocate
+ * nothing when called. Synchronizes the device if it allocates. */
+int tt_reserve(tt_handle handle, const tt_attn_desc* attn, int commit_B, int commit_L);
 
 /* Reads and clears the device status word. Synchronizes the handle's device
  * (cudaDeviceSynchronize). *device_status receives the TT_DEV_* bits (may be
- * NULL). Returns TT_OK if no bit was set, TT_ERR_DEVICE if one was, TT_ERR_CUDA
- * if the synchronization reported a CUDA error. */
-int tt_get_error(tt_handle handle, unsigned* device_status);
+ * NULL). After a timeout it also zeroes the handle's counters (a call that
+ * gave up may have left tickets behind). Returns TT_OK if no bit was set,
+ * TT_ERR_TIMEOUT if a wait timed out, TT_ERR_DEVICE_CHECK if only an argument
+ * check failed, TT_ERR_CUDA if the synchronization reported a CUDA error. */
+int tt_get_error(tt_handle handle, int* device_status);
 
 /* Sets how long a pipeline wait inside a kernel may last before it gives up,
  * sets TT_DEV_WAIT_TIMEOUT and lets the kernel wind down (default 1 s). */
 int tt_set_wait_timeout(tt_handle handle, unsigned long long nanoseconds);
+
+/* Tuning of the attention schedule (all attention entry points; results
+ * agree within the attention tolerance whatever the schedule).
+ *   kernel: 0 = chosen by shape (the default): the persistent schedule for
+ *           caches of 16384 positions or more outside the training layout,
+ *           one unit per CTA otherwise; 1 = one unit per CTA; 2 = persistent.
+ *   max_ctas, min_tiles (persistent schedule): at most max_ctas CTAs (0 = one
+ *           per SM) and at least min_tiles KV tiles of 128 keys per group of
+ *           CTAs (0 = the default, 8; 1 cuts at any tile).
+ *   splits (one-unit-per-CTA schedule): KV splits per unit (0 = by shape).
+ * A unit is (sequence, KV head, pair of 128-row query tiles). */
+int tt_set_attn_schedule(tt_handle handle, int kernel, int max_ctas, int min_tiles, int splits);
 
 /* Human-readable name of a tt_status value. */
 const char* tt_status_string(int status);
@@ -101,20 +133,9 @@ const char* tt_last_error(void);
  * Supported: D in {64, 128}; Hq % Hkv == 0 with Hq/Hkv a power of two <= 128;
  * 1 <= L <= 65536; B >= 0 (B == 0 is a no-op); scale > 0 or 0 for 1/sqrt(D).
  * ------------------------------------------------------------------------ */
-typedef struct {
-    int B, L, Hq, Hkv, D, ctx_cap;
-    float scale;    /* softmax scale; 0 selects 1/sqrt(D) */
-    int num_splits; /* KV splits per (b, kv head, query tile); 0 = automatic */
-} tt_attn_desc;
-
-/* Workspace bytes tt_block_attn needs for `desc` on this handle's device
- * (0 when no KV split is used). Returns 0 for an invalid desc as well. */
-size_t tt_block_attn_workspace_bytes(tt_handle handle, const tt_attn_desc* desc);
-
 int tt_block_attn(tt_handle handle, const tt_attn_desc* desc, const void* q, const void* k_blk,
                   const void* v_blk, const void* k_ctx, const void* v_ctx,
-                  const int32_t* ctx_len, void* out, void* workspace, size_t workspace_bytes,
-                  void* stream);
+                  const int32_t* ctx_len, void* out, void* stream);
 
 /* ------------------------------------------------------------------------
  * Context-tower update after a commit -- Section 2.1, Algorithm 1: once a
@@ -124,15 +145,14 @@ int tt_block_attn(tt_handle handle, const tt_attn_desc* desc, const void* q, con
  * tt_kv_append.
  *
  * tt_block_attn_causal: the same call as tt_block_attn (same arguments,
- * layouts, arithmetic, workspace and errors) except that block query l sees
+ * layouts, arithmetic and errors) except that block query l sees
  * the ctx_len[b] cache positions and block keys 0..l only:
  *   out[b][l][h] = softmax over [K_ctx[0..C_b-1]; K_blk[0..l]] applied to V.
  * With L == 1 it equals tt_block_attn (one autoregressive decode row).
  * ------------------------------------------------------------------------ */
 int tt_block_attn_causal(tt_handle handle, const tt_attn_desc* desc, const void* q,
                          const void* k_blk, const void* v_blk, const void* k_ctx,
-                         const void* v_ctx, const int32_t* ctx_len, void* out, void* workspace,
-                         size_t workspace_bytes, void* stream);
+                         const void* v_ctx, const int32_t* ctx_len, void* out, void* stream);
 
 /* tt_kv_append: copies the block's keys and values into the cache behind the
  * positions already there and advances the lengths:
@@ -140,12 +160,12 @@ int tt_block_attn_causal(tt_handle handle, const tt_attn_desc* desc, const void*
  *   ctx_len[b] += L
  * for every b with 0 <= ctx_len[b] <= ctx_cap - L. A block that does not fit
  * is skipped (cache and ctx_len[b] unchanged) and sets TT_DEV_CTX_LEN_RANGE.
- * desc gives B, L, Hkv, D and ctx_cap (Hq, scale and num_splits are not used);
+ * desc gives B, L, Hkv, D and ctx_cap (Hq and scale are not used);
  * layouts as for tt_block_attn: k_blk/v_blk [B][L][Hkv][D] bf16, k_ctx/v_ctx
  * [B][Hkv][ctx_cap][D] bf16 (written), ctx_len [B] int32 (read and written),
  * all device pointers, 16-byte aligned. Cache rows outside the appended range
  * are not touched. Two launches on `stream` (the copy, then the lengths), no
- * workspace. Supported: D in {64, 128}, 1 <= L <= ctx_cap, Hkv >= 1, B >= 0.
+ * scratch. Supported: D in {64, 128}, 1 <= L <= ctx_cap, Hkv >= 1, B >= 0.
  * Host errors: TT_ERR_INVALID_ARG for a NULL or misaligned pointer or a
  * descriptor outside the supported range.
  * ------------------------------------------------------------------------ */
@@ -172,20 +192,15 @@ int tt_kv_append(tt_handle handle, const tt_attn_desc* desc, const void* k_blk, 
  *   v_clean  [B][Hkv][N][D]     only positions below the block's start are read
  *   out      [B][N][Hq][D]
  * Supported: as tt_block_attn with L = S; N a multiple of S; B*N/S <= 65535.
- * Workspace: tt_block_attn_train_workspace_bytes (0 when no KV split is used).
  * ------------------------------------------------------------------------ */
 typedef struct {
     int B, N, S, Hq, Hkv, D;
-    float scale;    /* softmax scale; 0 selects 1/sqrt(D) */
-    int num_splits; /* KV splits per (block, kv head, query tile); 0 = automatic */
+    float scale; /* softmax scale; 0 selects 1/sqrt(D) */
 } tt_train_desc;
-
-size_t tt_block_attn_train_workspace_bytes(tt_handle handle, const tt_train_desc* desc);
 
 int tt_block_attn_train(tt_handle handle, const tt_train_desc* desc, const void* q,
                         const void* k_noisy, const void* v_noisy, const void* k_clean,
-                        const void* v_clean, void* out, void* workspace, size_t workspace_bytes,
-                        void* stream);
+                        const void* v_clean, void* out, void* stream);
 
 /* ------------------------------------------------------------------------
  * Unmask / commit -- Section 2.2, "Sampling", Algorithm 2 (ConfidenceSample),
@@ -209,20 +224,21 @@ int tt_block_attn_train(tt_handle handle, const tt_train_desc* desc, const void*
  *   masked_out [B*L] uint8, device; may be the same buffer as masked
  * Rows with masked[r] == 0 are not read. Supported: V % 4 == 0,
  * 4 <= V <= 131072, 1 <= L <= 16384, k >= 1 (k >= #masked commits all).
- * Workspace (tt_commit_workspace_bytes, 256-byte aligned): uint64 key[B*L] at
- * offset 0, int32 arg[B*L] at offset align256(8*B*L), uint32 ticket[B] at
- * align256(8*B*L) + align256(4*B*L). key/arg hold, after the call, the key and
- * prediction of every row that was masked on entry. The tickets must be ZERO
- * before a workspace is first used (e.g. cudaMemset); every call leaves them
- * zero again, so a workspace is zeroed once, not per call. After a call that
- * set TT_DEV_WAIT_TIMEOUT the tickets are undefined: zero them again.
- * Calls that share a workspace must not overlap on the GPU.
+ * masked and masked_out are the same buffer or do not overlap
+ * (TT_ERR_INVALID_ARG otherwise). The key and prediction of every row that was
+ * masked on entry stay in the handle's scratch until the next call on the
+ * handle (tt_commit_keys copies them out).
  * ------------------------------------------------------------------------ */
-size_t tt_commit_workspace_bytes(int B, int L);
-
 int tt_commit(tt_handle handle, const float* logits, int B, int L, int V, const uint8_t* masked,
-              int k, int32_t* tok, uint8_t* masked_out, void* workspace, size_t workspace_bytes,
-              void* stream);
+              int k, int32_t* tok, uint8_t* masked_out, void* stream);
+
+/* Copies the keys (uint64 [rows]) and predictions (int32 [rows]) that the last
+ * tt_commit / tt_commit_threshold call on this handle computed into device
+ * buffers key_dst / arg_dst (either may be NULL), asynchronously on `stream`.
+ * Entries of rows that were not masked in that call are unspecified. rows =
+ * B*L of that call. A debugging and testing aid (the canonical keys are what
+ * the committed set is decided on). */
+int tt_commit_keys(tt_handle handle, uint64_t* key_dst, int32_t* arg_dst, int rows, void* stream);
 
 /* ------------------------------------------------------------------------
  * Unmask / commit with a confidence threshold -- Section 2.2, Algorithm 2,
@@ -237,36 +253,44 @@ int tt_commit(tt_handle handle, const float* logits, int B, int L, int V, const 
  * the first ones of the (key, row) order, so the committed set is the first
  * max(#passing, ceil(#masked / steps_left)) masked rows of each block in that
  * order. gamma <= 0 commits every masked row; gamma >= 1 reduces to the floor.
- * Arguments, layouts, workspace and errors as tt_commit; gamma must not be NaN
+ * Arguments, layouts, scratch and errors as tt_commit; gamma must not be NaN
  * and steps_left must be >= 1.
  * ------------------------------------------------------------------------ */
 int tt_commit_threshold(tt_handle handle, const float* logits, int B, int L, int V,
                         const uint8_t* masked, double gamma, int steps_left, int32_t* tok,
-                        uint8_t* masked_out, void* workspace, size_t workspace_bytes,
-                        void* stream);
+                        uint8_t* masked_out, void* stream);
 
 /* ------------------------------------------------------------------------
  * Allocation-free commit. The paper has no counterpart of this entry point:
  * it is the same step as tt_commit, for callers that cannot allocate device
  * memory -- a serving engine that reserves all of HBM for its own pool at
  * start-up, or a plug-in host that forbids allocation while a request runs --
- * and so can neither call cudaMalloc nor provide a zero-filled workspace.
+ * and so can neither call cudaMalloc nor create a handle (whose scratch is
+ * allocated).
  *
- * Arguments and results are those of tt_commit without the handle and the
- * workspace; the scratch (per-row keys and predictions, per-block tickets)
- * is a fixed 1 MiB array built into the library, present on every GPU that
- * loads it until the process exits. Limits: B*L <= 65536 (larger sizes
- * return TT_ERR_UNSUPPORTED with a message in tt_last_error), plus those of
- * tt_commit. Works on the current CUDA device. The first call on a device
- * sets that device up (looks up the array's device address, sets kernel
- * attributes); make that first call before any stream capture. Each call
- * clears the tickets on `stream` (cudaMemsetAsync) and allocates nothing.
+ * Arguments and results are those of tt_commit without the handle; the
+ * scratch (per-row keys and predictions, per-block tickets, a status word)
+ * is a fixed array of about 1 MiB built into the library, present on every
+ * GPU that loads it until the process exits. Limits: B*L <= 65536 (larger
+ * sizes return TT_ERR_UNSUPPORTED with a message in tt_last_error), plus
+ * those of tt_commit. Works on the current CUDA device. The first call on a
+ * device sets that device up (looks up the array's device address, sets
+ * kernel attributes); with CUDA's lazy module loading that first call may
+ * also load the library's device code and so allocate, so make it (or a
+ * warm-up call) at start-up and before any stream capture. Later calls clear
+ * the tickets on `stream` (cudaMemsetAsync) and allocate nothing.
  * All calls share the one array: calls whose GPU work overlaps (other
- * streams, other threads) race and must be ordered by the caller. Device-side
- * wait timeouts are not reported (there is no handle status word).
+ * streams, other threads) race and must be ordered by the caller.
  * ------------------------------------------------------------------------ */
 int tt_commit_noalloc(const float* logits, int B, int L, int V, const uint8_t* masked, int k,
                       int32_t* tok, uint8_t* masked_out, void* stream);
+
+/* Reads and clears the status word of tt_commit_noalloc's built-in scratch on
+ * the current device (TT_DEV_* bits: a wait that timed out makes that call's
+ * outputs invalid). Synchronizes the device. Returns TT_OK, TT_ERR_TIMEOUT
+ * (the timeout bit was set; the tickets are cleared by the next call anyway)
+ * or TT_ERR_CUDA. The device must have made a tt_commit_noalloc call. */
+int tt_commit_noalloc_status(int* device_status);
 
 #ifdef __cplusplus
 }

@@ -34,24 +34,32 @@ def test_exports_every_declared_symbol(tt):
 
 def test_host_argument_errors(tt):
     lib = tt.lib()
-    assert lib.tt_commit_workspace_bytes(4, 32) == 1024 + 512 + 16
-    assert lib.tt_commit_workspace_bytes(-1, 3) == 0
     assert lib.tt_status_string(-2) == b"TT_ERR_UNSUPPORTED"
+    assert lib.tt_status_string(-4) == b"TT_ERR_TIMEOUT"
+    assert lib.tt_status_string(-5) == b"TT_ERR_DEVICE_CHECK"
     # NULL handle is rejected before anything else
-    rc = lib.tt_commit(None, None, 1, 1, 4, None, 1, None, None, None, 0, None)
+    rc = lib.tt_commit(None, None, 1, 1, 4, None, 1, None, None, None)
     assert rc == -1 and b"handle" in lib.tt_last_error()
-    d = tt.AttnDesc(1, 8, 4, 1, 64, 16, 0.0, 0)
-    assert lib.tt_block_attn(None, ctypes.byref(d), *([None] * 7), None, 0, None) == -1
-    assert lib.tt_block_attn_workspace_bytes(None, ctypes.byref(d)) == 0
+    rc = lib.tt_commit_threshold(None, None, 1, 1, 4, None, 0.8, 1, None, None, None)
+    assert rc == -1
+    d = tt.AttnDesc(1, 8, 4, 1, 64, 16, 0.0)
+    assert lib.tt_block_attn(None, ctypes.byref(d), *([None] * 7), None) == -1
     assert lib.tt_create(None, 0) == -1
+    assert lib.tt_reserve(None, ctypes.byref(d), 1, 1) == -1
+    assert lib.tt_set_attn_schedule(None, 0, 0, 0, 0) == -1
+    assert lib.tt_commit_keys(None, None, None, 1, None) == -1
+    assert lib.tt_get_error(None, None) == -1
     # the context-tower update and the training layout check the handle first too
-    assert lib.tt_block_attn_causal(None, ctypes.byref(d), *([None] * 7), None, 0, None) == -1
+    assert lib.tt_block_attn_causal(None, ctypes.byref(d), *([None] * 7), None) == -1
     assert lib.tt_kv_append(None, ctypes.byref(d), *([None] * 5), None) == -1
     assert b"tt_kv_append" in lib.tt_last_error()
-    t = tt.TrainDesc(1, 64, 16, 4, 1, 64, 0.0, 0)
-    assert lib.tt_block_attn_train(None, ctypes.byref(t), *([None] * 6), None, 0, None) == -1
+    t = tt.TrainDesc(1, 64, 16, 4, 1, 64, 0.0)
+    assert lib.tt_block_attn_train(None, ctypes.byref(t), *([None] * 6), None) == -1
     assert b"tt_block_attn_train" in lib.tt_last_error()
-    assert lib.tt_block_attn_train_workspace_bytes(None, ctypes.byref(t)) == 0
+    # the allocation-free commit checks its size bound before touching a device
+    assert lib.tt_commit_noalloc(None, 257, 256, 4, None, 1, None, None, None) == -2
+    assert b"65536" in lib.tt_last_error()
+    assert lib.tt_commit_noalloc(None, 1, 1, 4, None, 0, None, None, None) == -1
 
 
 def test_create_without_gpu_fails_cleanly(tt):

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 from block_diffusion_decoding_attn_b300 import workload as wl
+from conftest import KERNELS, SCHEDULES, attn_schedule
 
 pytestmark = pytest.mark.gpu
 
@@ -66,13 +67,36 @@ def test_small_cases(tt, oracle_lib, case):
     _assert_close(got, ref)
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7])
-def test_forced_splits_merge(tt, oracle_lib, splits):
+@pytest.mark.parametrize("sched", SCHEDULES)
+def test_schedules_cut_and_merge(tt, oracle_lib, sched):
+    # query tiles cut between CTAs at every tile boundary, merged by the last piece
     w = wl.custom("splits", 2, 32, 16, 2, 128, 1100, (1100, 45), qk_std=0.5)
     inp = wl.attn_inputs(w, seed=2)
-    got, _ = _run_gpu(tt, inp, num_splits=splits)
+    with attn_schedule(tt, *sched):
+        got, _ = _run_gpu(tt, inp)
     ref = oracle_lib.block_attn(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx, inp.v_ctx, inp.ctx_len)
     _assert_close(got, ref)
+
+
+@pytest.mark.parametrize("sched", [(2, 0, 1, 0), (2, 5, 1, 0), (2, 12, 2, 0), (1, 0, 0, 0), (1, 0, 0, 3)])
+def test_schedules_pair_groups(tt, oracle_lib, sched):
+    # 8 query tiles per (b, kv head): pair blocks of several CTAs, ragged lengths
+    w = wl.custom("groups", 3, 64, 32, 2, 128, 900, (900, 3, 517), qk_std=0.5)
+    inp = wl.attn_inputs(w, seed=6)
+    with attn_schedule(tt, *sched):
+        got, _ = _run_gpu(tt, inp)
+    ref = oracle_lib.block_attn(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx, inp.v_ctx, inp.ctx_len)
+    _assert_close(got, ref)
+
+
+def test_deterministic_under_one_schedule(tt):
+    w = wl.custom("det", 2, 32, 16, 2, 128, 1100, (1100, 45), qk_std=0.5)
+    inp = wl.attn_inputs(w, seed=2)
+    for sched in ((2, 0, 1, 0), (1, 0, 0, 3)):
+        with attn_schedule(tt, *sched):
+            a, _ = _run_gpu(tt, inp)
+            b, _ = _run_gpu(tt, inp)
+        assert np.array_equal(a, b)
 
 
 def test_cache_is_not_modified(tt):
@@ -81,8 +105,9 @@ def test_cache_is_not_modified(tt):
     inp = wl.attn_inputs(w, seed=3, pad=wl.to_bf16_bits(np.float32([7.0]))[0])
     t = wl.attn_tensors(inp)
     before = (t["k_ctx"].view(torch.int16).sum().item(), t["v_ctx"].view(torch.int16).sum().item())
-    tt.block_attn(t["q"], t["k_blk"], t["v_blk"], t["k_ctx"], t["v_ctx"], t["ctx_len"],
-                  num_splits=2)
+    for sched in ((2, 0, 1, 0), (1, 0, 0, 2)):
+        with attn_schedule(tt, *sched):
+            tt.block_attn(t["q"], t["k_blk"], t["v_blk"], t["k_ctx"], t["v_ctx"], t["ctx_len"])
     torch.cuda.synchronize()
     after = (t["k_ctx"].view(torch.int16).sum().item(), t["v_ctx"].view(torch.int16).sum().item())
     assert before == after
@@ -100,42 +125,27 @@ def test_ctx_len_out_of_range_is_flagged(tt):
     assert tt.handle().get_error() == 0  # cleared by the read
 
 
-def _sample_rows(w, ctx, n, seed):
-    rng = np.random.default_rng(seed)
-    rows = np.stack([rng.integers(0, w.B, n), rng.integers(0, w.L, n), rng.integers(0, w.Hq, n)], 1)
-    # always include the longest and the shortest sequence, first and last position
-    bl, bs = int(np.argmax(ctx)), int(np.argmin(ctx))
-    extra = np.array([[bl, 0, 0], [bl, w.L - 1, w.Hq - 1], [bs, 0, w.Hq - 1], [bs, w.L - 1, 0]])
-    return np.concatenate([rows, extra]).astype(np.int32)
-
-
-@pytest.mark.parametrize("name", ["tiny_c256_l32", "b8_c4096_l32", "b16_c1024_l256"])
+@pytest.mark.parametrize("name", ["tiny_c256_l32", "b8_c4096_l32", "b16_c1024_l256",
+                                  "b64_ragged8k32k_l64"])
 def test_full_workloads_all_rows(tt, oracle_lib, name):
+    # every output row against the oracle, with each of the two schedules
     w = wl.WORKLOADS[name]
     inp = wl.attn_inputs(w, seed=0)
-    got, _ = _run_gpu(tt, inp)
     ref = oracle_lib.block_attn(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx, inp.v_ctx, inp.ctx_len)
-    _assert_close(got, ref)
+    for sched in KERNELS:
+        with attn_schedule(tt, *sched):
+            got, _ = _run_gpu(tt, inp)
+        _assert_close(got, ref)
 
 
-def test_gen8k_schedule_sampled(tt, oracle_lib):
+def test_gen8k_schedule_every_call_all_rows(tt, oracle_lib):
+    # the 32 calls of the 8K-token generation (context 1024, 1280, ..., 8960)
     w = wl.WORKLOADS["b4_gen8k_32x256"]
-    for call in (0, 13, 31):
+    for call in range(len(w.ctx_schedule)):
         inp = wl.attn_inputs(w, seed=0, call=call)
-        got, _ = _run_gpu(tt, inp)
-        assert np.isfinite(got).all()
-        rows = _sample_rows(w, inp.ctx_len, 48, call)
         ref = oracle_lib.block_attn(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx, inp.v_ctx,
-                                    inp.ctx_len, rows=rows)
-        _assert_close(got[rows[:, 0], rows[:, 1], rows[:, 2]], ref)
-
-
-def test_ragged_long_context_sampled(tt, oracle_lib):
-    w = wl.WORKLOADS["b64_ragged8k32k_l64"]
-    inp = wl.attn_inputs(w, seed=0)
-    got, _ = _run_gpu(tt, inp)
-    assert np.isfinite(got).all()
-    rows = _sample_rows(w, inp.ctx_len, 96, 7)
-    ref = oracle_lib.block_attn(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx, inp.v_ctx, inp.ctx_len,
-                                rows=rows)
-    _assert_close(got[rows[:, 0], rows[:, 1], rows[:, 2]], ref)
+                                    inp.ctx_len)
+        for sched in KERNELS:
+            with attn_schedule(tt, *sched):
+                got, _ = _run_gpu(tt, inp)
+            _assert_close(got, ref)

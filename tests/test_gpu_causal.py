@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 
 from block_diffusion_decoding_attn_b300 import workload as wl
+from conftest import KERNELS, attn_schedule
 
 pytestmark = pytest.mark.gpu
 
@@ -72,19 +73,27 @@ def test_small_cases(tt, oracle_lib, case):
     _assert_close(_run_gpu(tt, inp), _oracle(oracle_lib, inp))
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 5])
-def test_forced_splits_with_fully_masked_tiles(tt, oracle_lib, splits):
-    # 3 context tiles + 2 block tiles: with 5 splits the last split holds only
-    # block keys 128..199, none of which rows l < 128 may see (m = -inf there).
+@pytest.mark.parametrize("sched", [(0, 0, 0, 0), (2, 1, 1, 0), (2, 2, 1, 0), (2, 3, 1, 0), (2, 0, 1, 0),
+                                   (1, 0, 0, 2), (1, 0, 0, 3), (1, 0, 0, 5)])
+def test_cut_pieces_with_fully_masked_tiles(tt, oracle_lib, sched):
+    # 3 context tiles + 2 block tiles per unit: with one-tile pieces, a piece
+    # holding only block keys 128..199 has no key that rows l < 128 may see
+    # (m = -inf there); the merge gives it weight 0.
     w = wl.custom("splits", 2, 200, 4, 2, 128, 384, (384, 300), qk_std=0.5)
     inp = wl.attn_inputs(w, seed=2)
-    _assert_close(_run_gpu(tt, inp, num_splits=splits), _oracle(oracle_lib, inp))
+    with attn_schedule(tt, *sched):
+        got = _run_gpu(tt, inp)
+    _assert_close(got, _oracle(oracle_lib, inp))
 
 
-def test_no_context_split_per_block_tile(tt, oracle_lib):
+def test_no_context_one_piece_per_block_tile(tt, oracle_lib):
     w = wl.custom("blk_only", 2, 256, 8, 1, 64, 128, (0, 0), qk_std=0.5)
     inp = wl.attn_inputs(w, seed=3)
-    _assert_close(_run_gpu(tt, inp, num_splits=2), _oracle(oracle_lib, inp))
+    ref = _oracle(oracle_lib, inp)
+    for sched in ((2, 0, 1, 0), (1, 0, 0, 2)):
+        with attn_schedule(tt, *sched):
+            got = _run_gpu(tt, inp)
+        _assert_close(got, ref)
 
 
 def test_last_row_matches_bidirectional_call(tt):
@@ -100,30 +109,22 @@ def test_last_row_matches_bidirectional_call(tt):
     assert not torch.equal(ca[:, 0], bi[:, 0])
 
 
-def _sample_rows(w, ctx, n, seed):
-    rng = np.random.default_rng(seed)
-    rows = np.stack([rng.integers(0, w.B, n), rng.integers(0, w.L, n), rng.integers(0, w.Hq, n)], 1)
-    bl, bs = int(np.argmax(ctx)), int(np.argmin(ctx))
-    extra = np.array([[bl, 0, 0], [bl, w.L - 1, w.Hq - 1], [bs, 0, w.Hq - 1], [bs, w.L - 1, 0],
-                      [bl, 127, 3], [bs, 128, 5]]) % np.array([w.B, w.L, w.Hq])
-    return np.concatenate([rows, extra]).astype(np.int32)
-
-
 def test_full_workload_l256_all_rows(tt, oracle_lib):
     w = wl.WORKLOADS["b16_c1024_l256"]
     inp = wl.attn_inputs(w, seed=0)
     _assert_close(_run_gpu(tt, inp), _oracle(oracle_lib, inp))
 
 
-def test_gen8k_schedule_sampled(tt, oracle_lib):
+def test_gen8k_schedule_every_call_all_rows(tt, oracle_lib):
+    # the context tower's pass over each of the 32 committed blocks
     w = wl.WORKLOADS["b4_gen8k_32x256"]
-    for call in (0, 31):
+    for call in range(len(w.ctx_schedule)):
         inp = wl.attn_inputs(w, seed=0, call=call)
-        got = _run_gpu(tt, inp)
-        assert np.isfinite(got).all()
-        rows = _sample_rows(w, inp.ctx_len, 48, call)
-        ref = _oracle(oracle_lib, inp, rows=rows)
-        _assert_close(got[rows[:, 0], rows[:, 1], rows[:, 2]], ref)
+        ref = _oracle(oracle_lib, inp)
+        for sched in KERNELS:
+            with attn_schedule(tt, *sched):
+                got = _run_gpu(tt, inp)
+            _assert_close(got, ref)
 
 
 # ---------------------------------------------------------------- K/V append

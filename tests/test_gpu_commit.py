@@ -31,10 +31,10 @@ def _gpu_step(tt, logits, B, L, masked, k, tok, alias=False):
     m = torch.from_numpy(masked.copy()).cuda()
     t = torch.from_numpy(tok.copy()).cuda()
     mo = m if alias else None
-    t, mo, ws = tt.commit(lg, B, L, m, k, t, masked_out=mo)
+    t, mo = tt.commit(lg, B, L, m, k, t, masked_out=mo)
+    keys, args = tt.commit_keys(B * L)
     torch.cuda.synchronize()
     assert tt.handle().get_error() == 0
-    keys, args = tt.commit_keys(ws, B, L)
     return (t.cpu().numpy(), mo.cpu().numpy(), keys.cpu().numpy().view(np.uint64),
             args.cpu().numpy())
 
@@ -126,6 +126,46 @@ def test_full_workloads_first_step(tt, oracle_lib, name):
     w = wl.WORKLOADS[name]
     inp = wl.commit_inputs(w, seed=0)
     _check_step(tt, oracle_lib, inp.logits, w.B, w.L, inp.masked, w.k, inp.tok)
+
+
+@pytest.mark.parametrize("alias", [False, True], ids=["separate", "in_place"])
+@pytest.mark.parametrize("name", ["b4_gen8k_32x256", "b64_ragged8k32k_l64"])
+def test_full_workloads_ragged_mask(tt, oracle_lib, name, alias):
+    # a later denoising step: about half of each block still masked, a different
+    # set per block, so cluster shares start and end inside blocks and include
+    # unmasked rows; in place, the mask is rewritten while other clusters run
+    w = wl.WORKLOADS[name]
+    lg = wl.logits(w, seed=0, step=3)
+    masked = wl.random_mask(w, 0.5, seed=17)
+    tok = np.where(masked == 1, -1, np.arange(w.rows) % w.V).astype(np.int32)
+    _check_step(tt, oracle_lib, lg, w.B, w.L, masked, w.k, tok, alias=alias)
+
+
+def test_canonical_key_at_reduction_boundaries(tt, oracle_lib):
+    # Differences l - max at which rounding x*log2(e) to fp32 first would move
+    # the exponential's n by one (the product is within half an fp32 ulp of a
+    # half-integer): the keys must still agree with the oracle bit for bit.
+    l2e = np.float32(1.0 / 0.69314718055994530942)
+    xs = []
+    for k in range(44):
+        x0 = np.float32(-(k + 0.5) / float(l2e))
+        for d in range(-40, 41):
+            x = np.array([x0.view(np.int32) + d], np.int32).view(np.float32)[0]
+            if -30.0 <= x <= 0.0:
+                xs.append(x)
+    xs = np.array(xs, np.float32)
+    V = 4096
+    rows = -(-len(xs) // (V - 1))
+    w = wl.custom("bnd", 1, max(rows, 2), 1, 1, 8, 8, (0,), V=V, k=1)
+    lg = wl.logits(w, seed=21) - np.float32(40.0)   # every other term is 0
+    flat = lg.reshape(-1)
+    for r in range(w.rows):
+        lg[r, 0] = 0.0                                 # the row maximum
+        chunk = xs[r * (V - 1):(r + 1) * (V - 1)]
+        lg[r, 1:1 + len(chunk)] = chunk                # l - max = x exactly
+    assert flat.size == w.rows * V
+    masked = np.ones(w.rows, np.uint8)
+    _check_step(tt, oracle_lib, lg, 1, w.rows, masked, 1, np.full(w.rows, -1, np.int32))
 
 
 def test_b8_full_loop(tt, oracle_lib):

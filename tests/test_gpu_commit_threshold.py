@@ -30,10 +30,10 @@ def _check(tt, oracle_lib, logits, B, L, masked, gamma, steps_left, tok):
     lg = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
     m = torch.from_numpy(masked.copy()).cuda()
     t = torch.from_numpy(tok.copy()).cuda()
-    t, mo, ws = tt.commit_threshold(lg, B, L, m, gamma, steps_left, t)
+    t, mo = tt.commit_threshold(lg, B, L, m, gamma, steps_left, t)
+    gk, ga = tt.commit_keys(B * L)
     torch.cuda.synchronize()
     assert tt.handle().get_error() == 0
-    gk, ga = tt.commit_keys(ws, B, L)
     gk, ga = gk.cpu().numpy().view(np.uint64), ga.cpu().numpy()
     ot, om, ok, oa = oracle_lib.commit_threshold(logits, B, L, masked, gamma, steps_left, tok)
     sel = masked == 1

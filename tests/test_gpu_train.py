@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 from block_diffusion_decoding_attn_b300 import workload as wl
+from conftest import KERNELS, attn_schedule
 
 pytestmark = pytest.mark.gpu
 
@@ -69,24 +70,23 @@ def test_small_cases(tt, oracle_lib, case):
     _assert_close(_run_gpu(tt, inp, S), _oracle(oracle_lib, inp, S))
 
 
-@pytest.mark.parametrize("splits", [2, 5])
-def test_forced_splits(tt, oracle_lib, splits):
+@pytest.mark.parametrize("sched", [(2, 2, 1, 0), (2, 5, 1, 0), (2, 0, 1, 0), (1, 0, 0, 2), (1, 0, 0, 5)])
+def test_cut_pieces(tt, oracle_lib, sched):
     inp = _inputs(2, 1024, 16, 2, 128, seed=2, qk_std=0.5)
-    _assert_close(_run_gpu(tt, inp, 16, num_splits=splits), _oracle(oracle_lib, inp, 16))
+    with attn_schedule(tt, *sched):
+        got = _run_gpu(tt, inp, 16)
+    _assert_close(got, _oracle(oracle_lib, inp, 16))
 
 
-def test_paper_block_size_full_length_sampled(tt, oracle_lib):
+def test_paper_block_size_full_length_all_rows(tt, oracle_lib):
     # S = 16 (the final configuration of Section 2.3), 4096 tokens, 256 blocks
     B, N, S = 2, 4096, 16
     inp = _inputs(B, N, 32, 2, 128, seed=0)
-    got = _run_gpu(tt, inp, S)
-    assert np.isfinite(got).all()
-    rng = np.random.default_rng(4)
-    rows = np.stack([rng.integers(0, B, 80), rng.integers(0, N, 80), rng.integers(0, 32, 80)], 1)
-    rows = np.concatenate([rows, [[0, 0, 0], [1, N - 1, 31], [0, S - 1, 5], [1, S, 6]]])
-    rows = rows.astype(np.int32)
-    ref = _oracle(oracle_lib, inp, S, rows=rows)
-    _assert_close(got[rows[:, 0], rows[:, 1], rows[:, 2]], ref)
+    ref = _oracle(oracle_lib, inp, S)
+    for sched in KERNELS:
+        with attn_schedule(tt, *sched):
+            got = _run_gpu(tt, inp, S)
+        _assert_close(got, ref)
 
 
 def test_invalid_block_size_raises(tt):
