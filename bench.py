@@ -412,6 +412,13 @@ def time_schedule(tt, h, stream, flush, w, calls, Cm, out, m_out, rounds, warm):
     return t_attn, t_comm
 
 
+def attn_schedule_name(w):
+    """The attention schedule the library picks for workload w (by cache size)."""
+    if w.ctx_cap >= 16384:
+        return "one persistent stream-K attention kernel, cut query tiles merged in it"
+    return "one-unit-per-CTA attention kernel (+ the split merge when a unit is split)"
+
+
 def roof_attention(w, inps, a_ms, peaks, name):
     ncalls = len(inps)
     fl = sum(attn_flops(w, inp.ctx_len) for inp in inps) / ncalls
@@ -420,7 +427,7 @@ def roof_attention(w, inps, a_ms, peaks, name):
     per = "per call" if ncalls == 1 else f"per call, mean over the {ncalls} calls of a step"
     return {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": tf / peaks["bf16_tflops"], "traffic": profiled_traffic("block_attn", name),
-            "kernel": "tt_block_attn call (one persistent attention kernel, pieces merged in it)",
+            "kernel": f"tt_block_attn call ({attn_schedule_name(w)})",
             "algorithmic": f"{fl:.4g} FLOP, {by:.4g} B {per}", "ms": a_ms,
             "peak_source": peaks["source"] + " burst"}
 
@@ -463,7 +470,8 @@ def run_gpu(args, w):
     m_out = torch.empty_like(Cm["masked"])
     h.reserve(tt.attn_desc(As[0]["q"], As[0]["k_ctx"]), w.B, w.L)  # no allocation while timing
     ncalls = len(As)
-    launches_per_step = ncalls * 2  # one attention and one commit launch per call
+    # per call: the attention kernel (+ a merge kernel when a unit is split), one commit kernel
+    launches_per_step = ncalls * (tt.block_attn_launches(tt.attn_desc(As[0]["q"], As[0]["k_ctx"]), h) + 1)
 
     K = args.steps
     with ClockSampler(local) as clk:
@@ -609,6 +617,52 @@ def run_gpu(args, w):
                                            for i in range(2, Ku + 2)), dist)
     del Tt, out_t
 
+    # The denoiser's LM head at the pages' width (K = 2688) over the step's
+    # rows, then the commit given the row maxima its epilogue found, against
+    # the same LM head followed by the commit that finds them itself: whether
+    # folding the row maximum into the GEMM epilogue pays.
+    K_lm = wl.LM_HIDDEN
+    _, w_np = wl.lm_head_inputs(1, K_lm, w.V, seed=rank)
+    w_t = torch.from_numpy(w_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    del w_np
+
+    def lm_leg(B_, L_, k_):
+        """(LM head ms, commit given the row maxima ms, commit finding them ms)
+        over B_ blocks of L_ rows, fully masked."""
+        rows_ = B_ * L_
+        hid_np, _ = wl.lm_head_inputs(rows_, K_lm, 4, seed=rank)
+        hid_t = torch.from_numpy(hid_np.view(np.int16)).to(dev).view(torch.bfloat16)
+        lg_t = Cm["logits"][:rows_]  # the step's logits buffer, [rows][V]
+        m_lm = torch.ones(rows_, dtype=torch.uint8, device=dev)
+        mo_lm = torch.empty_like(m_lm)
+        t_lm = torch.full((rows_,), -1, dtype=torch.int32, device=dev)
+        rounds = max(2, min(K, 4))
+        evm = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(rounds + 1)]
+        for i in range(rounds + 1):  # the first round warms up
+            flush()
+            evm[i][0].record(stream)
+            tt.lm_head(hid_t, w_t, logits=lg_t, h=h, stream=stream)
+            evm[i][1].record(stream)
+            flush()
+            evm[i][2].record(stream)
+            tt.commit_rowmax(lg_t, B_, L_, m_lm, k_, t_lm, masked_out=mo_lm, h=h, stream=stream)
+            evm[i][3].record(stream)
+            flush()
+            evm[i][4].record(stream)
+            tt.commit(lg_t, B_, L_, m_lm, k_, t_lm, masked_out=mo_lm, h=h, stream=stream)
+            evm[i][5].record(stream)
+        torch.cuda.synchronize()
+        if h.get_error():
+            raise RuntimeError("device status set during the LM-head leg")
+        return tuple(max_over_ranks(statistics.mean(evm[i][a].elapsed_time(evm[i][a + 1])
+                                                    for i in range(1, rounds + 1)), dist)
+                     for a in (0, 2, 4))
+
+    gemm_ms, crm_ms, ccl_ms = lm_leg(w.B, w.L, w.k)
+    ws_ = wl.WORKLOADS[SCHEDULE_WORKLOAD]
+    lm_short = lm_leg(ws_.B, ws_.L, ws_.k) if ws_.V == w.V and ws_.rows <= w.rows else None
+    del w_t
+
     # The 8K-token generation schedule (32 calls, context growing by one
     # block each call), per-call attention and commit, when it is not the
     # step's own workload.
@@ -666,9 +720,34 @@ def run_gpu(args, w):
                   "algorithmic": f"{fl_t:.4g} FLOP (visible pairs) per call",
                   "ms": tr_ms, "tokens_per_s": TRAIN_B * TRAIN_N / (tr_ms * 1e-3),
                   "peak_source": peaks["source"] + " burst"}
+    gemm_fl = 2.0 * w.rows * K_lm * w.V
+    gemm_tf = gemm_fl / (gemm_ms * 1e-3) / 1e12
+    by_lm = commit_bytes(w, w.rows)
+    crm_gbs = by_lm / (crm_ms * 1e-3) / 1e9
+    roof_lm = {
+        "bound": "tensor", "achieved": gemm_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+        "frac": gemm_tf / peaks["bf16_tflops"], "traffic": None,
+        "kernel": f"tt_lm_head: logits [{w.rows}][{w.V}] = hidden [{w.rows}][{K_lm}] x weight^T, "
+                  "row max / first argmax folded into the epilogue; outside the step",
+        "algorithmic": f"{gemm_fl:.4g} FLOP per call", "ms": gemm_ms,
+        "peak_source": peaks["source"] + " burst",
+        "commit_given_rowmax": {"bound": "hbm", "achieved": crm_gbs, "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": crm_gbs / peaks["hbm_gbs"], "ms": crm_ms,
+                                "kernel": "tt_commit_rowmax (fully masked block)",
+                                "algorithmic": f"{by_lm:.4g} B per call"},
+        "commit_finding_rowmax_ms": ccl_ms,
+        "lm_head_plus_commit_ms": {"folded row max": gemm_ms + crm_ms, "separate": gemm_ms + ccl_ms},
+    }
+    if lm_short:
+        ws_ = wl.WORKLOADS[SCHEDULE_WORKLOAD]
+        roof_lm[f"{ws_.rows}_rows ({SCHEDULE_WORKLOAD}'s commit shape)"] = {
+            "lm_head_ms": lm_short[0], "commit_given_rowmax_ms": lm_short[1],
+            "commit_finding_rowmax_ms": lm_short[2],
+            "commit_given_rowmax_frac_hbm": commit_bytes(ws_, ws_.rows) / (lm_short[1] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "commit_finding_rowmax_frac_hbm": commit_bytes(ws_, ws_.rows) / (lm_short[2] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     dom = roof_attn if a_ms >= c_ms else roof_comm
     kernels = {"attention": roof_attn, "commit": roof_comm, "commit_full_loop": roof_loop,
-               "context_update": roof_upd, "train_attention": roof_train}
+               "context_update": roof_upd, "train_attention": roof_train, "lm_head": roof_lm}
     if sched:
         kernels[SCHEDULE_WORKLOAD] = sched
     line = {
@@ -695,6 +774,70 @@ def run_gpu(args, w):
     return 0
 
 
+PROFILE_CASES = ("attn_gen8k_call16", "attn_ragged_slice16", "commit_gen8k", "commit_ragged",
+                 "lm_head_commit")
+
+
+def run_profile_case(case):
+    """One small case of one kernel, run twice (warm, then the one to capture
+    with ncu -s 1 -c 1), each after an L2 flush: the inputs stay a few GB at
+    most, larger than L2.
+
+    attn_gen8k_call16    block attention, b4_gen8k_32x256 call 16 (context 5120)
+    attn_ragged_slice16  block attention, the first 16 sequences of b64_ragged8k32k_l64
+    commit_gen8k         commit step, b4_gen8k_32x256 (1024 rows, fully masked)
+    commit_ragged        commit step, b64_ragged8k32k_l64 (4096 rows, fully masked)
+    lm_head_commit       LM head (1024 rows, K = 2688, V = 32768) and the commit behind it
+    """
+    import torch
+    import block_diffusion_decoding_attn_b300 as tt
+    from block_diffusion_decoding_attn_b300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = L2Flush(dev)
+    if case.startswith("attn"):
+        if case == "attn_gen8k_call16":
+            w = wl.WORKLOADS["b4_gen8k_32x256"]
+            t = wl.attn_tensors(wl.attn_inputs(w, seed=0, call=16), dev)
+        else:
+            w = wl.WORKLOADS["b64_ragged8k32k_l64"]
+            ws = wl.Workload("ragged_slice16", w.wid, B=16, L=w.L, Hq=w.Hq, Hkv=w.Hkv, D=w.D,
+                             ctx_cap=w.ctx_cap, V=w.V, k=w.k, ctx_range=w.ctx_range)
+            t = wl.attn_tensors(wl.attn_inputs(ws, seed=0), dev)
+        out = torch.empty_like(t["q"])
+        for _ in range(2):
+            flush()
+            tt.block_attn(t["q"], t["k_blk"], t["v_blk"], t["k_ctx"], t["v_ctx"], t["ctx_len"], out=out)
+            torch.cuda.synchronize()
+    elif case == "lm_head_commit":
+        M, K, V, L = 1024, wl.LM_HIDDEN, 32768, 64
+        hid, wt = wl.lm_head_inputs(M, K, V, seed=0)
+        hid = torch.from_numpy(hid.view(np.int16)).to(dev).view(torch.bfloat16)
+        wt = torch.from_numpy(wt.view(np.int16)).to(dev).view(torch.bfloat16)
+        lg = torch.empty((M, V), dtype=torch.float32, device=dev)
+        m = torch.ones(M, dtype=torch.uint8, device=dev)
+        tok = torch.full((M,), -1, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            flush()
+            tt.lm_head(hid, wt, logits=lg)
+            flush()
+            tt.commit_rowmax(lg, M // L, L, m, 8, tok, masked_out=torch.empty_like(m))
+            torch.cuda.synchronize()
+    else:
+        w = wl.WORKLOADS["b4_gen8k_32x256" if case == "commit_gen8k" else "b64_ragged8k32k_l64"]
+        c = wl.commit_tensors(wl.commit_inputs(w, seed=0), dev)
+        mo = torch.empty_like(c["masked"])
+        for _ in range(2):
+            flush()
+            tt.commit(c["logits"], w.B, w.L, c["masked"], w.k, c["tok"].clone(), masked_out=mo)
+            torch.cuda.synchronize()
+    if tt.handle(0).get_error():
+        raise RuntimeError("device status set")
+    print(f"profile case {case} ok")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -703,7 +846,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="run one small case of one kernel twice (for an ncu capture) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args.profile_case)
     if args.warmup < 3:
         args.warmup = 3
     w = wl.WORKLOADS[args.workload]

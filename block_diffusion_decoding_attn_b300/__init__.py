@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             L.tt_status_string.argtypes = [I]
             L.tt_last_error.restype = ctypes.c_char_p
             L.tt_last_error.argtypes = []
+            L.tt_block_attn_launches.argtypes = [P, ctypes.POINTER(AttnDesc)]
             L.tt_block_attn.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 7 + [P]
             L.tt_block_attn_causal.argtypes = L.tt_block_attn.argtypes
             L.tt_kv_append.argtypes = [P, ctypes.POINTER(AttnDesc)] + [P] * 5 + [P]
@@ -77,12 +78,14 @@ def lib() -> ctypes.CDLL:
             L.tt_commit_threshold.argtypes = [P, P, I, I, I, P, ctypes.c_double, I, P, P, P]
             L.tt_commit_keys.argtypes = [P, P, P, I, P]
             L.tt_commit_noalloc.argtypes = [P, I, I, I, P, I, P, P, P]
+            L.tt_lm_head.argtypes = [P, P, P, I, I, I, P, P]
+            L.tt_commit_rowmax.argtypes = [P, P, I, I, I, P, I, P, P, P]
             L.tt_commit_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
             for f in ("tt_create", "tt_destroy", "tt_get_error", "tt_set_wait_timeout",
-                      "tt_set_attn_schedule", "tt_reserve", "tt_block_attn",
+                      "tt_set_attn_schedule", "tt_reserve", "tt_block_attn", "tt_block_attn_launches",
                       "tt_block_attn_causal", "tt_kv_append", "tt_block_attn_train", "tt_commit",
                       "tt_commit_threshold", "tt_commit_keys", "tt_commit_noalloc",
-                      "tt_commit_noalloc_status"):
+                      "tt_commit_noalloc_status", "tt_lm_head", "tt_commit_rowmax"):
                 getattr(L, f).restype = I
             _lib = L
     return _lib
@@ -185,6 +188,15 @@ def attn_desc(q, k_ctx, scale: float = 0.0) -> AttnDesc:
     B, L, Hq, D = q.shape
     Hkv, C = k_ctx.shape[1], k_ctx.shape[2]
     return AttnDesc(B, L, Hq, Hkv, D, C, float(scale))
+
+
+def block_attn_launches(desc: AttnDesc, h: Handle | None = None) -> int:
+    """Kernel launches one attention call with this descriptor makes (1 or 2)."""
+    h = h or handle()
+    n = int(lib().tt_block_attn_launches(h.ptr, ctypes.byref(desc)))
+    if n < 0:
+        _check(n, "tt_block_attn_launches")
+    return n
 
 
 def block_attn(q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out=None, scale: float = 0.0,
@@ -329,3 +341,40 @@ def commit_keys(rows: int, h: Handle | None = None, device=None, stream=None):
     _check(lib().tt_commit_keys(h.ptr, _dev_ptr(keys), _dev_ptr(args), int(rows),
                                 ctypes.c_void_p(st.cuda_stream)), "tt_commit_keys")
     return keys, args
+
+
+def lm_head(hidden, weight, logits=None, h: Handle | None = None, stream=None):
+    """The denoiser's LM head: logits = hidden @ weight^T (bf16 in, fp32 out) on
+    the tensor core; each row's maximum and prediction stay in the handle for
+    :func:`commit_rowmax`. hidden [M][K], weight [V][K] (torch.bfloat16, CUDA,
+    contiguous). Returns logits [M][V] float32."""
+    import torch
+    for name, t in (("hidden", hidden), ("weight", weight)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    M, K = hidden.shape
+    V = weight.shape[0]
+    if weight.shape[1] != K:
+        raise ValueError("lm_head: hidden and weight disagree on K")
+    h = h or handle(hidden.device.index)
+    if logits is None:
+        logits = torch.empty((M, V), dtype=torch.float32, device=hidden.device)
+    _check(lib().tt_lm_head(h.ptr, _dev_ptr(hidden), _dev_ptr(weight), int(M), int(K), int(V),
+                            _dev_ptr(logits), _stream_ptr(hidden, stream)), "tt_lm_head")
+    return logits
+
+
+def commit_rowmax(logits, B: int, L: int, masked, k: int, tok, masked_out=None,
+                  h: Handle | None = None, stream=None):
+    """The commit step on the logits of the last :func:`lm_head` call on the
+    handle, with the row maxima it found (tt_commit_rowmax). Arguments and
+    results as :func:`commit`."""
+    import torch
+    _check_commit_args(logits, masked, tok)
+    h = h or handle(logits.device.index)
+    if masked_out is None:
+        masked_out = torch.empty_like(masked)
+    _check(lib().tt_commit_rowmax(h.ptr, _dev_ptr(logits), int(B), int(L), int(logits.shape[1]),
+                                  _dev_ptr(masked), int(k), _dev_ptr(tok), _dev_ptr(masked_out),
+                                  _stream_ptr(logits, stream)), "tt_commit_rowmax")
+    return tok, masked_out

@@ -11,8 +11,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libtt.so")
 SOURCES = ["tt_api.cu", "block_attn.cu", "block_attn_split.cu", "commit.cu", "commit_noalloc.cu",
-           "kv_append.cu"]
-HEADERS = ["ptx.cuh", "tt_internal.h"]
+           "kv_append.cu", "lm_head.cu"]
+HEADERS = ["ptx.cuh", "tt_internal.h", "commit_select.cuh", "commit_key.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -36,22 +36,11 @@
 //       commits.
 // Pass 1 and the exchange of row i + 1 run while pass 2 works on row i.
 
-// e(x) is an fp32 exponential defined for this purpose (Cody and Waite range
-// reduction, then the degree-7 Taylor polynomial of exp, all with
-// round-to-nearest fused multiply-adds):
-//   x < -30 -> term 0
-//   n = nearest integer (ties to even) to the exact product x * log2(e)
-//   r = fma(-n, C1, x), r = fma(-n, C2, r)     C1 = RN32(ln 2), C2 = RN32(ln 2 - C1)
-//   p = c7; p = fma(p, r, c_j), j = 6..0       c_j = RN32(1 / j!)
-//   term = rint(p * 2^(n + 40))
-// The term is formed without any float-to-64-bit conversion (those run on the
-// FP64 pipe, which is narrow on this part): the polynomial carries the 2^40
-// factor in its coefficients (exact power-of-two scaling), 2^n is added to the
-// exponent field, and rint splits into a multiple of 2^20 plus a remainder,
-// both read out of the bits of exact fp32 sums. The arithmetic runs on packed
-// f32x2 pairs (each half rounded exactly like the scalar operation).
+// The canonical key and its exponential: commit_key.cuh.
 #include <atomic>
 
+#include "commit_key.cuh"
+#include "commit_select.cuh"
 #include "ptx.cuh"
 #include "tt_internal.h"
 
@@ -59,21 +48,7 @@ namespace tt {
 
 namespace {
 
-// RN32(1/ln 2), RN32(ln 2), RN32(ln 2 - RN32(ln 2)); 2^40 * RN32(1/j!)
-constexpr float kLog2e = 0x1.715476p+0f;
-constexpr float kLn2Hi = 0x1.62e430p-1f;
-constexpr float kLn2Lo = -0x1.05c610p-29f;
-constexpr float kC0 = 0x1.000000p+40f;
-constexpr float kC2 = 0x1.000000p+39f;
-constexpr float kC3 = 0x1.555556p+37f;
-constexpr float kC4 = 0x1.555556p+35f;
-constexpr float kC5 = 0x1.111112p+33f;
-constexpr float kC6 = 0x1.6c16c2p+30f;
-constexpr float kC7 = 0x1.a01a02p+27f;
-constexpr float kMagic23 = 0x1.8p+23f;  // fp32 sums in [2^23, 2^24) have ulp 1
-constexpr float kMagic43 = 0x1.8p+43f;  // ... in [2^43, 2^44) have ulp 2^20
-constexpr unsigned kMagic23Bits = 0x4B400000u;
-constexpr unsigned kMagic43Bits = 0x55400000u;
+using namespace key;
 
 constexpr int kSlots = 3;                 // ring depth: 64 KB chunks landing per CTA
 constexpr int kChunk = 16384;             // logits per ring slot
@@ -90,88 +65,9 @@ constexpr int kP1PerChunk = kChunk / kP1Threads;    // logits per pass-1 thread 
 constexpr int kP2Cols = kRowCols / (kP2Warps / 4);  // TMEM columns per pass-2 thread
 constexpr int kThreads = (kSumSenderWarp + 1) * 32;
 constexpr int kXchg = 8;                  // exchange slots (rows in flight in the cluster)
-constexpr int kSelChunk = 2048;           // keys staged per selection pass
+using sel::kSelChunk;                     // keys staged per selection pass
 static_assert(kSliceMax == kCommitSliceMax, "slice per CTA");
 static_assert(2 * kRowCols == 512, "two row slots fill the TMEM");
-
-// Packed fp32 pairs: one f32x2 instruction does the same round-to-nearest
-// operation on both halves, halving the issue slots of the term arithmetic.
-using f2 = unsigned long long;
-
-__device__ __forceinline__ f2 pk(float a, float b) {
-    f2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void upk(f2 r, float& a, float& b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ f2 dup(float c) { return pk(c, c); }
-__device__ __forceinline__ f2 ffma2(f2 a, f2 b, f2 c) {
-    f2 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ f2 fadd2(f2 a, f2 b) {
-    f2 d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f2 fsub2(f2 a, f2 b) {
-    f2 d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// Adds the fixed-point terms of x0, x1 (RN32(l - m) clamped below at -31;
-// terms below -28.4 round to 0 either way) to the accumulators:
-//   sum of terms = (hi - cnt * kMagic43Bits) * 2^20 + (lo - cnt * kMagic23Bits)
-// (mod 2^32 each), with cnt the number of terms added; the constant offsets
-// are taken out once at the end.
-__device__ __forceinline__ void add_terms(f2 x, unsigned& hi, unsigned& lo) {
-    const f2 nb = ffma2(x, dup(kLog2e), dup(kMagic23));  // 1.5*2^23 + n
-    const f2 n = fsub2(nb, dup(kMagic23));
-    f2 r = ffma2(n, dup(-kLn2Hi), x);
-    r = ffma2(n, dup(-kLn2Lo), r);
-    f2 p = ffma2(dup(kC7), r, dup(kC6));
-    p = ffma2(p, r, dup(kC5));
-    p = ffma2(p, r, dup(kC4));
-    p = ffma2(p, r, dup(kC3));
-    p = ffma2(p, r, dup(kC2));
-    p = ffma2(p, r, dup(kC0));
-    p = ffma2(p, r, dup(kC0));  // 2^40 * p(r), in [2^39.5, 2^40.5]
-    float p0, p1, nb0, nb1;
-    upk(p, p0, p1);
-    upk(nb, nb0, nb1);
-    // y = p * 2^n: add n to the exponent field; (bits(nb) << 23) == (n << 23) mod 2^32.
-    const f2 y = pk(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(nb0) << 23)),
-                    __uint_as_float(__float_as_uint(p1) + (__float_as_uint(nb1) << 23)));
-    const f2 a = fadd2(y, dup(kMagic43));               // 1.5*2^43 + 2^20 * round(y / 2^20)
-    const f2 rem = fsub2(y, fsub2(a, dup(kMagic43)));   // exact, |rem| <= 2^19
-    const f2 b = fadd2(rem, dup(kMagic23));             // 1.5*2^23 + rint(rem)
-    float a0, a1, b0, b1;
-    upk(a, a0, a1);
-    upk(b, b0, b1);
-    hi += __float_as_uint(a0) + __float_as_uint(a1);
-    lo += __float_as_uint(b0) + __float_as_uint(b1);
-}
-
-// (value, index) as one orderable 64-bit word: a larger value wins, equal
-// values go to the lower index. -0.0 is folded into +0.0 first (they compare
-// equal). 0 is below every encoded pair.
-__device__ __forceinline__ unsigned long long enc_argmax(float v, int i) {
-    unsigned u = __float_as_uint(v + 0.0f);
-    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - static_cast<unsigned>(i));
-}
-__device__ __forceinline__ float dec_value(unsigned long long e) {
-    unsigned u = static_cast<unsigned>(e >> 32);
-    u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
-    return __uint_as_float(u);
-}
-__device__ __forceinline__ int dec_index(unsigned long long e) {
-    return static_cast<int>(0xFFFFFFFFu - static_cast<unsigned>(e));
-}
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
@@ -244,175 +140,6 @@ struct CommitShared {
     int wsum[kThreads / 32];  // start-up scan: masked rows per warp
     uint32_t tmem;          // TMEM base address (512 columns)
 };
-
-// Commits the k most confident masked rows of block b: tok[r] = arg[r],
-// masked_out[r] = 0; the block's other masked rows get masked_out[r] = 1
-// (unmasked rows are written by the row's owner). Order: (key, row)
-// ascending. Every masked row of the block has written its key and
-// prediction (the block's last ticket was taken); reads go through L2. Run by
-// one warp. All masked flags are read before any write, since masked_out may
-// alias masked. n = number of masked rows in the block.
-//   n <= k: every masked row commits, no ranking;
-//   L <= kSelChunk: k rounds of a warp argmin over the keys staged in shared
-//       memory, each round taking the smallest (key, row) above the last;
-//   larger L: each row's rank is counted over the keys, chunk by chunk.
-// Rows block b commits, given its n masked rows and, in threshold mode, the
-// number of them whose key is <= kthr (cthr, the rows whose confidence is
-// above gamma: they are the first cthr rows of the (key, row) order).
-__device__ __forceinline__ int block_budget(const CommitParams& p, int n, int cthr) {
-    if (p.steps_left <= 0) return p.k;
-    return max(cthr, (n + p.steps_left - 1) / p.steps_left);
-}
-
-// L <= 256: every lane holds up to 8 rows (row 32 q + lane) in registers;
-// flags, keys and predictions come in one round trip of loads.
-constexpr int kSelRegRows = 8;
-
-__device__ void select_block_small(const CommitParams& p, int b, int n, int lane) {
-    const size_t base = static_cast<size_t>(b) * p.L;
-    bool mi[kSelRegRows];
-    unsigned long long ki[kSelRegRows];
-    int ai[kSelRegRows];
-#pragma unroll
-    for (int q = 0; q < kSelRegRows; ++q) {
-        const int i = q * 32 + lane;
-        mi[q] = false;
-        ki[q] = ~0ull;
-        ai[q] = 0;
-        if (i < p.L) {
-            mi[q] = __ldcg(p.masked + base + i) != 0;
-            ki[q] = __ldcg(p.key + base + i);
-            ai[q] = __ldcg(p.arg + base + i);
-        }
-    }
-    int cthr = 0;
-#pragma unroll
-    for (int q = 0; q < kSelRegRows; ++q) {
-        if (!mi[q]) ki[q] = ~0ull;  // unmasked rows never rank
-        cthr += (mi[q] && ki[q] <= p.kthr) ? 1 : 0;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cthr += __shfl_xor_sync(0xffffffffu, cthr, o);
-    const int kb = block_budget(p, n, cthr);
-    uint32_t commit = 0;  // bit q: row 32 q + lane is committed
-#pragma unroll
-    for (int q = 0; q < kSelRegRows; ++q)
-        if (n <= kb && mi[q]) commit |= 1u << q;
-    if (n > kb) {
-        unsigned long long lk = 0;  // last chosen (key, row); row -1: none yet
-        int lr = -1;
-        for (int round = 0; round < kb; ++round) {
-            unsigned long long bk = ~0ull;
-            int br = 0x7fffffff;
-#pragma unroll
-            for (int q = 0; q < kSelRegRows; ++q) {
-                const int j = q * 32 + lane;
-                const bool above = ki[q] > lk || (ki[q] == lk && j > lr);
-                const bool below = ki[q] < bk || (ki[q] == bk && j < br);
-                if (ki[q] != ~0ull && above && below) { bk = ki[q]; br = j; }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const unsigned long long ok_ = __shfl_xor_sync(0xffffffffu, bk, o);
-                const int orow = __shfl_xor_sync(0xffffffffu, br, o);
-                if (ok_ < bk || (ok_ == bk && orow < br)) { bk = ok_; br = orow; }
-            }
-            if (br == 0x7fffffff) break;
-            if ((br & 31) == lane) commit |= 1u << (br >> 5);
-            lk = bk;
-            lr = br;
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < kSelRegRows; ++q) {
-        const int i = q * 32 + lane;
-        if (mi[q]) {
-            const bool c = (commit >> q) & 1u;
-            if (c) p.tok[base + i] = ai[q];
-            p.masked_out[base + i] = c ? 0 : 1;
-        }
-    }
-}
-
-__device__ void select_block(const CommitParams& p, int b, int n, unsigned long long* s_key,
-                             uint32_t* s_mbits, uint32_t* s_cbits, int lane) {
-    const size_t base = static_cast<size_t>(b) * p.L;
-    const int nw = (p.L + 31) / 32;
-    int cthr = 0;
-    for (int w = 0; w < nw; ++w) {
-        const int i = w * 32 + lane;
-        const bool mi = i < p.L && __ldcg(p.masked + base + i) != 0;
-        cthr += (mi && p.steps_left > 0 && __ldcg(p.key + base + i) <= p.kthr) ? 1 : 0;
-        const uint32_t mb = __ballot_sync(0xffffffffu, mi);
-        if (lane == 0) s_mbits[w] = mb;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cthr += __shfl_xor_sync(0xffffffffu, cthr, o);
-    const int kb = block_budget(p, n, cthr);
-    if (lane == 0)
-        for (int w = 0; w < nw; ++w) s_cbits[w] = n <= kb ? s_mbits[w] : 0u;
-    __syncwarp();
-    if (n > kb && p.L <= kSelChunk) {
-        for (int j = lane; j < p.L; j += 32)
-            s_key[j] = (s_mbits[j >> 5] >> (j & 31)) & 1u ? __ldcg(p.key + base + j) : ~0ull;
-        __syncwarp();
-        unsigned long long lk = 0;  // last chosen (key, row); row -1: none yet
-        int lr = -1;
-        for (int round = 0; round < kb; ++round) {
-            unsigned long long bk = ~0ull;
-            int br = 0x7fffffff;
-            for (int j = lane; j < p.L; j += 32) {
-                const unsigned long long kj = s_key[j];
-                const bool above = kj > lk || (kj == lk && j > lr);
-                const bool below = kj < bk || (kj == bk && j < br);
-                if (kj != ~0ull && above && below) { bk = kj; br = j; }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const unsigned long long ok_ = __shfl_xor_sync(0xffffffffu, bk, o);
-                const int orow = __shfl_xor_sync(0xffffffffu, br, o);
-                if (ok_ < bk || (ok_ == bk && orow < br)) { bk = ok_; br = orow; }
-            }
-            if (br == 0x7fffffff) break;
-            if (lane == 0) s_cbits[br >> 5] |= 1u << (br & 31);
-            lk = bk;
-            lr = br;
-        }
-    } else if (n > kb) {
-        for (int w = 0; w < nw; ++w) {
-            const int i = w * 32 + lane;
-            const bool mi = (s_mbits[w] >> lane) & 1u;
-            const unsigned long long ki = mi ? __ldcg(p.key + base + i) : 0ull;
-            int rank = 0;
-            for (int j0 = 0; j0 < p.L; j0 += kSelChunk) {
-                const int cn = min(kSelChunk, p.L - j0);
-                __syncwarp();
-                for (int j = lane; j < cn; j += 32)
-                    s_key[j] = (s_mbits[(j0 + j) >> 5] >> ((j0 + j) & 31)) & 1u
-                                   ? __ldcg(p.key + base + j0 + j)
-                                   : ~0ull;
-                __syncwarp();
-                const int lim = i - j0;  // rows j0 + j < i win ties
-                for (int j = 0; j < cn; ++j) {
-                    const unsigned long long kj = s_key[j];
-                    rank += (kj < ki || (kj == ki && j < lim)) ? 1 : 0;
-                }
-            }
-            const uint32_t cb = __ballot_sync(0xffffffffu, mi && rank < kb);
-            if (lane == 0) s_cbits[w] = cb;
-        }
-    }
-    __syncwarp();
-    for (int w = 0; w < nw; ++w) {
-        const int i = w * 32 + lane;
-        if ((s_mbits[w] >> lane) & 1u) {
-            const bool c = (s_cbits[w] >> lane) & 1u;
-            if (c) p.tok[base + i] = __ldcg(p.arg + base + i);
-            p.masked_out[base + i] = c ? 0 : 1;
-        }
-    }
-    __syncwarp();
-}
 
 __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* a, unsigned v) {
     unsigned old;
@@ -626,8 +353,8 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (__shfl_sync(0xffffffffu, last, 0)) {
                     __threadfence();  // every lane reads the other clusters' rows after the ticket
-                    if (p.L <= 32 * kSelRegRows) select_block_small(p, cb, cnum, lane);
-                    else select_block(p, cb, cnum, s_key, s_mbits, s_cbits, lane);
+                    if (p.L <= 32 * sel::kSelRegRows) sel::select_block_small(p, cb, cnum, lane);
+                    else sel::select_block(p, cb, cnum, s_key, s_mbits, s_cbits, lane);
                 }
             };
             const int total = sh.total;

@@ -40,6 +40,12 @@ struct tt_context {
     };
     MapEntry maps[32];
     unsigned long long map_clock;
+    // LM head -> commit hand-off: per-row maxima and key accumulators [rows]
+    // (u64 each) and block tickets [blocks] (u32), zero between calls; the
+    // shape of the last tt_lm_head call.
+    void* lm;
+    size_t lm_rows, lm_blocks;
+    int lm_M, lm_V;
 };
 
 namespace {
@@ -332,6 +338,7 @@ int tt_create(tt_handle* out, int device) {
     if ((e = tt::configure_attn_split_kernels()) != cudaSuccess)
         return cuda_fail(e, "attention kernel attributes");
     if ((e = tt::configure_commit_kernels()) != cudaSuccess) return cuda_fail(e, "commit kernel attributes");
+    if ((e = tt::configure_lm_head_kernels()) != cudaSuccess) return cuda_fail(e, "LM head kernel attributes");
     tt_context* h = new tt_context();
     h->device = device;
     h->num_sms = prop.multiProcessorCount;
@@ -366,6 +373,7 @@ int tt_destroy(tt_handle h) {
     cudaFree(h->status);
     if (h->ws) cudaFree(h->ws);
     if (h->ctr) cudaFree(h->ctr);
+    if (h->lm) cudaFree(h->lm);
     delete h;
     return TT_OK;
 }
@@ -409,6 +417,16 @@ int tt_reserve(tt_handle h, const tt_attn_desc* attn, int commit_B, int commit_L
     return ensure_workspace(h, ws, ctr);
 }
 
+int tt_block_attn_launches(tt_handle h, const tt_attn_desc* d) {
+    if (!h) return fail(TT_ERR_INVALID_ARG, "tt_block_attn_launches: handle is NULL");
+    AttnPlan pl;
+    const int st = plan_attn(d, h->num_sms, h->max_ctas, d ? d->B : 0, &pl);
+    if (st != TT_OK) return st;
+    if (d->B == 0) return 0;
+    if (use_persistent(h, d, 0)) return 1;
+    return plan_split(d, pl, h->num_sms, h->splits).splits > 1 ? 2 : 1;
+}
+
 int tt_get_error(tt_handle h, int* device_status) {
     if (!h) return fail(TT_ERR_INVALID_ARG, "handle is NULL");
     DeviceGuard g(h->device);
@@ -421,6 +439,9 @@ int tt_get_error(tt_handle h, int* device_status) {
     // A call that gave up on a wait may have left tickets behind.
     if ((v & TT_DEV_WAIT_TIMEOUT) && h->ctr &&
         (e = cudaMemset(h->ctr, 0, h->ctr_count * sizeof(unsigned))) != cudaSuccess)
+        return cuda_fail(e, "clear counters");
+    if ((v & TT_DEV_WAIT_TIMEOUT) && h->lm &&
+        (e = cudaMemset(h->lm, 0, h->lm_rows * 16 + h->lm_blocks * 4)) != cudaSuccess)
         return cuda_fail(e, "clear counters");
     if (device_status) *device_status = static_cast<int>(v);
     if (v & TT_DEV_WAIT_TIMEOUT) return TT_ERR_TIMEOUT;
@@ -708,6 +729,131 @@ int tt_commit_threshold(tt_handle h, const float* logits, int B, int L, int V,
     if (std::isnan(gamma)) return fail(TT_ERR_INVALID_ARG, "tt_commit_threshold: gamma is NaN");
     return commit_impl(h, "tt_commit_threshold", logits, B, L, V, masked, 1, steps_left,
                        key_threshold(gamma), tok, masked_out, stream);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- LM head and the commit behind it
+namespace {
+
+// Grows the LM head's hand-off buffer (zeroed) to `rows` rows, with room for
+// as many block tickets (a block has at least one row), so that the commit
+// behind an LM head never has to grow it (growing clears the row maxima).
+int ensure_lm(tt_context* h, size_t rows) {
+    if (rows <= h->lm_rows) return TT_OK;
+    const size_t r = rows, b = rows;
+    cudaError_t e;
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    if (h->lm) cudaFree(h->lm);
+    h->lm = nullptr;
+    h->lm_rows = h->lm_blocks = 0;
+    if ((e = cudaMalloc(&h->lm, r * 16 + b * 4)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(lm)");
+    if ((e = cudaMemset(h->lm, 0, r * 16 + b * 4)) != cudaSuccess) return cuda_fail(e, "cudaMemset(lm)");
+    h->lm_rows = r;
+    h->lm_blocks = b;
+    return TT_OK;
+}
+
+unsigned long long* lm_key(tt_context* h) { return static_cast<unsigned long long*>(h->lm); }
+unsigned long long* lm_rowmax(tt_context* h) { return static_cast<unsigned long long*>(h->lm) + h->lm_rows; }
+unsigned* lm_blk(tt_context* h) {
+    return reinterpret_cast<unsigned*>(static_cast<unsigned long long*>(h->lm) + 2 * h->lm_rows);
+}
+
+int encode2d(tt_context* h, CUtensorMap* m, const void* base, int inner, int outer, int box_outer,
+             const char* name) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t str[1] = {static_cast<cuuint64_t>(inner) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_outer)};
+    return encode_cached(h, m, const_cast<void*>(base), 2, dims, str, box, name);
+}
+
+}  // namespace
+
+extern "C" {
+
+int tt_lm_head(tt_handle h, const void* hidden, const void* weight, int M, int K, int V, float* logits,
+               void* stream) {
+    if (!h) return fail(TT_ERR_INVALID_ARG, "tt_lm_head: handle is NULL");
+    if (M < 0 || K < 8 || K % 8 || V < 4 || V % 4)
+        return fail(TT_ERR_INVALID_ARG, "tt_lm_head: needs M >= 0, K >= 8 with K %% 8 == 0, V >= 4 with V %% 4 == 0");
+    if (K > (1 << 20) || V > (1 << 24) || M > (1 << 24))
+        return fail(TT_ERR_UNSUPPORTED, "tt_lm_head: K, V or M too large");
+    if (M == 0) return TT_OK;
+    if (!hidden || !weight || !logits) return fail(TT_ERR_INVALID_ARG, "tt_lm_head: a tensor pointer is NULL");
+    if (!aligned16(hidden) || !aligned16(weight) || !aligned16(logits))
+        return fail(TT_ERR_INVALID_ARG, "tt_lm_head: tensors must be 16-byte aligned");
+    DeviceGuard g(h->device);
+    if (!g.ok()) return fail(TT_ERR_CUDA, "cannot select device %d", h->device);
+    int st = ensure_lm(h, static_cast<size_t>(M));
+    if (st != TT_OK) return st;
+    CUtensorMap ma, mb;
+    if ((st = encode2d(h, &ma, hidden, K, M, 128, "hidden")) != TT_OK) return st;
+    if ((st = encode2d(h, &mb, weight, K, V, 256, "weight")) != TT_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    // each row's maximum is an atomic max over the vocabulary tiles: from zero
+    if ((e = cudaMemsetAsync(lm_rowmax(h), 0, static_cast<size_t>(M) * 8, s)) != cudaSuccess)
+        return cuda_fail(e, "tt_lm_head: clear row maxima");
+    tt::LmHeadParams p;
+    p.M = M; p.K = K; p.V = V;
+    p.logits = logits;
+    p.rowmax = lm_rowmax(h);
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    if ((e = tt::launch_lm_head(ma, mb, p, h->num_sms, s)) != cudaSuccess)
+        return cuda_fail(e, "tt_lm_head launch");
+    h->lm_M = M;
+    h->lm_V = V;
+    return TT_OK;
+}
+
+static int commit_rowmax_impl(tt_handle h, const char* name, const float* logits, int B, int L, int V,
+                              const uint8_t* masked, int k, int steps_left, unsigned long long kthr,
+                              int32_t* tok, uint8_t* masked_out, void* stream) {
+    if (!h) return fail(TT_ERR_INVALID_ARG, "%s: handle is NULL", name);
+    if (B < 0 || L < 1 || L > tt::kCommitMaxL)
+        return fail(TT_ERR_INVALID_ARG, "%s: needs B >= 0 and 1 <= L <= %d", name, tt::kCommitMaxL);
+    if (B == 0) return TT_OK;
+    if (static_cast<long long>(B) * L != h->lm_M || V != h->lm_V)
+        return fail(TT_ERR_INVALID_ARG, "%s: B*L and V must be the M and V of the last tt_lm_head call", name);
+    if (!logits || !masked || !tok || !masked_out)
+        return fail(TT_ERR_INVALID_ARG, "%s: a tensor pointer is NULL", name);
+    if (!aligned16(logits)) return fail(TT_ERR_INVALID_ARG, "%s: logits must be 16-byte aligned", name);
+    const size_t rows = static_cast<size_t>(B) * L;
+    const uintptr_t mi = reinterpret_cast<uintptr_t>(masked), mo = reinterpret_cast<uintptr_t>(masked_out);
+    if (mi != mo && mi < mo + rows && mo < mi + rows)
+        return fail(TT_ERR_INVALID_ARG, "%s: masked and masked_out overlap without being the same buffer", name);
+    DeviceGuard g(h->device);
+    if (!g.ok()) return fail(TT_ERR_CUDA, "cannot select device %d", h->device);
+    int st = ensure_lm(h, rows);  // no growth: rows == the LM head's M
+    if (st != TT_OK) return st;
+    if ((st = ensure_workspace(h, commit_ws_bytes(rows), 0)) != TT_OK) return st;
+    tt::RowmaxCommitParams p;
+    p.logits = logits;
+    p.B = B; p.L = L; p.V = V; p.k = k;
+    p.steps_left = steps_left;
+    p.kthr = kthr;
+    p.masked = masked;
+    p.tok = tok;
+    p.masked_out = masked_out;
+    p.key = lm_key(h);
+    p.rowmax = lm_rowmax(h);
+    p.blk = lm_blk(h);
+    p.key_out = static_cast<unsigned long long*>(h->ws);
+    p.arg = reinterpret_cast<int32_t*>(static_cast<char*>(h->ws) + align256(rows * 8));
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    const cudaError_t e = tt::launch_commit_rowmax(p, h->num_sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    return TT_OK;
+}
+
+int tt_commit_rowmax(tt_handle h, const float* logits, int B, int L, int V, const uint8_t* masked, int k,
+                     int32_t* tok, uint8_t* masked_out, void* stream) {
+    if (k < 1) return fail(TT_ERR_INVALID_ARG, "tt_commit_rowmax: k=%d < 1", k);
+    return commit_rowmax_impl(h, "tt_commit_rowmax", logits, B, L, V, masked, k, 0, 0ull, tok, masked_out,
+                              stream);
 }
 
 }  // extern "C"

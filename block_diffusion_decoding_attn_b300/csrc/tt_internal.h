@@ -132,6 +132,43 @@ int commit_max_clusters();  // co-resident clusters of the commit kernel (curren
 cudaError_t configure_commit_kernels();
 cudaError_t configure_attn_kernels();
 
+// LM head: logits[M][V] = hidden[M][K] * W[V][K]^T (bf16 in, fp32 out) on the
+// tensor core; each row's maximum and first argmax go to rowmax (atomic max of
+// key::enc_argmax, zero before the call).
+struct LmHeadParams {
+    int M, K, V;
+    float* logits;
+    unsigned long long* rowmax;  // [M]
+    unsigned* status;
+    unsigned long long timeout_ns;
+};
+
+// The commit step given each row's maximum / prediction (rowmax) — the
+// fixed-budget or threshold rule as in CommitParams; key accumulates each
+// row's fixed-point terms (zero before the call, zero after), blk counts each
+// block's finished (row, chunk) units (zero before and after).
+struct RowmaxCommitParams {
+    const float* logits;
+    int B, L, V, k, steps_left;
+    unsigned long long kthr;
+    const uint8_t* masked;
+    int32_t* tok;
+    uint8_t* masked_out;
+    unsigned long long* key;     // [B*L] accumulators
+    unsigned long long* rowmax;  // [B*L] from the LM head; zeroed per completed block
+    unsigned* blk;               // [B]
+    int32_t* arg;                // [B*L] predictions (out)
+    unsigned long long* key_out; // [B*L] keys (out)
+    unsigned* status;
+    unsigned long long timeout_ns;
+};
+
+size_t lm_head_smem_bytes();
+cudaError_t configure_lm_head_kernels();
+cudaError_t launch_lm_head(const CUtensorMap& a, const CUtensorMap& b, const LmHeadParams& p, int num_sms,
+                           cudaStream_t s);
+cudaError_t launch_commit_rowmax(const RowmaxCommitParams& p, int num_sms, cudaStream_t s);
+
 // Records "<where>: <msg>" as the calling thread's last host error (tt_last_error).
 void record_host_error(const char* where, const char* msg);
 

@@ -39,6 +39,10 @@ import numpy as np
 
 # Tensor ids in the Philox key.
 _T_Q, _T_KBLK, _T_VBLK, _T_KCTX, _T_VCTX, _T_LOGITS, _T_CTXLEN = 1, 2, 3, 4, 5, 6, 7
+_T_HIDDEN, _T_WEIGHT = 8, 9
+
+# Hidden size of the denoiser's LM head (the pages' model width).
+LM_HIDDEN = 2688
 
 _CHUNK = 1 << 22  # elements per independently keyed chunk
 
@@ -255,3 +259,12 @@ def commit_tensors(inp: CommitInputs, device="cuda", pin: bool = False) -> dict:
         return x.to(device, non_blocking=pin) if device != "cpu" else x
 
     return dict(logits=t(inp.logits), masked=t(inp.masked), tok=t(inp.tok))
+
+
+def lm_head_inputs(M: int, K: int, V: int, seed: int = 0, wid: int = 200, step: int = 0):
+    """hidden [M][K] ~ N(0, 1) and weight [V][K] ~ N(0, 4/K) as bf16 bit patterns,
+    so that the logits hidden @ weight^T have variance about 4 (the logits'
+    recipe, N(0, 4)). `step` draws a fresh hidden state (a later denoising step)."""
+    hid = _fill_normal(M * K, 1.0, seed, wid, _T_HIDDEN + 16 * step, True).reshape(M, K)
+    w = _fill_normal(V * K, 2.0 / math.sqrt(K), seed, wid, _T_WEIGHT, True).reshape(V, K)
+    return hid, w

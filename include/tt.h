@@ -102,6 +102,12 @@ int tt_set_wait_timeout(tt_handle handle, unsigned long long nanoseconds);
  * A unit is (sequence, KV head, pair of 128-row query tiles). */
 int tt_set_attn_schedule(tt_handle handle, int kernel, int max_ctas, int min_tiles, int splits);
 
+/* Kernel launches a tt_block_attn / tt_block_attn_causal call with this
+ * descriptor makes on this handle under its current schedule (1, or 2 when a
+ * unit is split and merged by a second kernel); a negative tt_status for an
+ * invalid descriptor. */
+int tt_block_attn_launches(tt_handle handle, const tt_attn_desc* desc);
+
 /* Human-readable name of a tt_status value. */
 const char* tt_status_string(int status);
 
@@ -259,6 +265,32 @@ int tt_commit_keys(tt_handle handle, uint64_t* key_dst, int32_t* arg_dst, int ro
 int tt_commit_threshold(tt_handle handle, const float* logits, int B, int L, int V,
                         const uint8_t* masked, double gamma, int steps_left, int32_t* tok,
                         uint8_t* masked_out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The denoiser's LM head with the commit step behind it -- Section 2.2,
+ * Algorithm 2: the denoiser's distribution over the vocabulary for every
+ * position of the block, then ConfidenceSample on it.
+ *
+ * tt_lm_head: logits[m][v] = sum_k hidden[m][k] * weight[v][k], bf16 inputs,
+ * fp32 accumulation on the tensor core, fp32 logits out (written in full).
+ * Its epilogue also finds each row's maximum and first argmax and leaves
+ * them in the handle for the next tt_commit_rowmax call on the handle (a new
+ * tt_lm_head replaces them).
+ *   hidden [M][K] bf16, weight [V][K] bf16, logits [M][V] fp32; device
+ *   pointers, 16-byte aligned; K % 8 == 0, V % 4 == 0, K >= 8, V >= 4.
+ * Two launches (the row maxima are cleared first).
+ *
+ * tt_commit_rowmax: the same step as tt_commit (same rule, keys, tie-breaks,
+ * results, in-place masks allowed) on the logits of the last tt_lm_head call
+ * (B*L == its M, V == its V; TT_ERR_INVALID_ARG otherwise), using the row
+ * maxima and predictions it found instead of a pass of its own. One launch.
+ * The commit is bit-identical to tt_commit on the same logits.
+ * ------------------------------------------------------------------------ */
+int tt_lm_head(tt_handle handle, const void* hidden, const void* weight, int M, int K, int V,
+               float* logits, void* stream);
+
+int tt_commit_rowmax(tt_handle handle, const float* logits, int B, int L, int V,
+                     const uint8_t* masked, int k, int32_t* tok, uint8_t* masked_out, void* stream);
 
 /* ------------------------------------------------------------------------
  * Allocation-free commit. The paper has no counterpart of this entry point:

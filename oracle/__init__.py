@@ -17,6 +17,8 @@ method's arithmetic.
   of a clean sequence in one pass, block j attending to the clean positions
   before it and bidirectionally to itself (a loop over blocks of
   ``block_attn``).
+* ``lm_head`` is the denoiser's output layer before Section 2.2's sampling:
+  logits = hidden @ weight^T over bf16 values, in float64.
 * ``block_attn(..., causal=True)`` and ``kv_append`` follow Section 2.1,
   Algorithm 1 (the context update after a commit): the context tower's causal pass over a
   committed block, and its keys/values joining the prefix cache.
@@ -181,6 +183,24 @@ def kv_append(k_blk, v_blk, k_ctx, v_ctx, ctx_len):
                 v_new[b, h, c + l, :] = v_blk[b, l, h, :]
         n_new[b] = c + L
     return k_new, v_new, n_new.astype(np.int32), fits
+
+
+def bf16_to_f64(bits):
+    """bf16 bit patterns (uint16) widened exactly to float64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def lm_head(hidden, weight, rows=None):
+    """The denoiser's LM head, the step that produces the vocabulary logits
+    Section 2.2's sampling reads (Algorithm 2's distribution p_theta):
+    logits[m][v] = sum_k hidden[m][k] * weight[v][k], in float64 over the bf16
+    values (hidden [M][K], weight [V][K] as bf16 bit patterns). ``rows``: only
+    those rows of hidden."""
+    h = bf16_to_f64(hidden)
+    if rows is not None:
+        h = h[np.asarray(rows)]
+    return h @ bf16_to_f64(weight).T
 
 
 def exp_own(x: float) -> float:

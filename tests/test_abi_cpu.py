@@ -56,6 +56,10 @@ def test_host_argument_errors(tt):
     t = tt.TrainDesc(1, 64, 16, 4, 1, 64, 0.0)
     assert lib.tt_block_attn_train(None, ctypes.byref(t), *([None] * 6), None) == -1
     assert b"tt_block_attn_train" in lib.tt_last_error()
+    # the LM head and the commit behind it
+    assert lib.tt_lm_head(None, None, None, 1, 8, 4, None, None) == -1
+    assert lib.tt_commit_rowmax(None, None, 1, 1, 4, None, 1, None, None, None) == -1
+    assert lib.tt_block_attn_launches(None, ctypes.byref(d)) == -1
     # the allocation-free commit checks its size bound before touching a device
     assert lib.tt_commit_noalloc(None, 257, 256, 4, None, 1, None, None, None) == -2
     assert b"65536" in lib.tt_last_error()
