@@ -89,13 +89,18 @@ def load_peaks():
             "source": "fallback"}
 
 
-def file_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def sources_hash(paths):
+    """sha256 (16 hex digits) of the concatenated files, in the given order."""
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    sources are still the ones captured (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -104,8 +109,9 @@ def profiled_traffic(kernel, workload):
     e = t.get(kernel, {}).get(workload)
     if not e:
         return None
-    src = os.path.join(ROOT, e["source"])
-    if not os.path.exists(src) or file_hash(src) != e["source_sha256"]:
+    if not all(os.path.exists(os.path.join(ROOT, s)) for s in e["sources"]):
+        return None
+    if sources_hash(e["sources"]) != e["sources_sha256"]:
         return None  # the kernel changed since the counters were taken
     return e["dram_bytes_per_launch"]
 

@@ -41,7 +41,9 @@ import numpy as np
 _T_Q, _T_KBLK, _T_VBLK, _T_KCTX, _T_VCTX, _T_LOGITS, _T_CTXLEN = 1, 2, 3, 4, 5, 6, 7
 _T_HIDDEN, _T_WEIGHT = 8, 9
 
-# Hidden size of the denoiser's LM head (the pages' model width).
+# Input width of the denoiser's LM head. The pages name the backbone
+# (Nemotron-3-Nano-30B-A3B) but not its hidden size; 2688 is read as that
+# backbone's hidden size.
 LM_HIDDEN = 2688
 
 _CHUNK = 1 << 22  # elements per independently keyed chunk
