@@ -22,6 +22,8 @@ constexpr int kSelChunk = 2048;  // keys staged per selection pass (shared memor
 // one warp. All masked flags are read before any write, since masked_out may
 // alias masked. n = number of masked rows in the block.
 //   n <= k: every masked row commits, no ranking;
+//   L <= 256 (select_block_small): rounds of a warp minimum over per-lane
+//       sorted lists (binary search on the key for large budgets);
 //   L <= kSelChunk: k rounds of a warp argmin over the keys staged in shared
 //       memory, each round taking the smallest (key, row) above the last;
 //   larger L: each row's rank is counted over the keys, chunk by chunk.
@@ -34,73 +36,123 @@ __device__ __forceinline__ int block_budget(const P& p, int n, int cthr) {
     return max(cthr, (n + p.steps_left - 1) / p.steps_left);
 }
 
-// L <= 256: every lane holds up to 8 rows (row 32 q + lane) in registers;
-// flags, keys and predictions come in one round trip of loads.
+// L <= 256 (select_block_small): lane l holds rows 8 l .. 8 l + 7 in
+// registers (flags, keys and predictions in one round trip of loads). Up to
+// kSelRounds commits: each lane sorts its 8 (key, row) pairs, then every round
+// takes the warp minimum of the lanes' heads with three redux.sync minima
+// (key high word, key low word, lane: rows are lane-major, so the lowest lane
+// holds the lowest row among equal keys) and the winning lane pops its head.
+// More commits: a binary search for the kb-th smallest key with ballots, then
+// the tied rows at that key in row order.
 constexpr int kSelRegRows = 8;
+constexpr int kSelRounds = 96;
+
+__device__ __forceinline__ bool key_row_less(unsigned long long ka, int ra, unsigned long long kb,
+                                             int rb) {
+    return ka < kb || (ka == kb && ra < rb);
+}
 
 template <class P>
 __device__ void select_block_small(const P& p, int b, int n, int lane) {
     const size_t base = static_cast<size_t>(b) * p.L;
-    bool mi[kSelRegRows];
-    unsigned long long ki[kSelRegRows];
-    int ai[kSelRegRows];
+    unsigned long long key[kSelRegRows];
+    int arg[kSelRegRows];
+    uint32_t mbits = 0;  // bit q: row 8 lane + q is masked
+    {
+        uint8_t m[kSelRegRows];
+        unsigned long long k[kSelRegRows];
 #pragma unroll
-    for (int q = 0; q < kSelRegRows; ++q) {
-        const int i = q * 32 + lane;
-        mi[q] = false;
-        ki[q] = ~0ull;
-        ai[q] = 0;
-        if (i < p.L) {
-            mi[q] = __ldcg(p.masked + base + i) != 0;
-            ki[q] = __ldcg(p.key + base + i);
-            ai[q] = __ldcg(p.arg + base + i);
+        for (int q = 0; q < kSelRegRows; ++q) {
+            const int i = min(lane * kSelRegRows + q, p.L - 1);
+            m[q] = __ldcg(p.masked + base + i);
+            k[q] = __ldcg(p.key + base + i);
+            arg[q] = __ldcg(p.arg + base + i);
+        }
+#pragma unroll
+        for (int q = 0; q < kSelRegRows; ++q) {
+            const bool ok = lane * kSelRegRows + q < p.L && m[q] != 0;
+            mbits |= ok ? (1u << q) : 0u;
+            key[q] = ok ? k[q] : ~0ull;  // a masked row's key is below 2^63
         }
     }
     int cthr = 0;
 #pragma unroll
-    for (int q = 0; q < kSelRegRows; ++q) {
-        if (!mi[q]) ki[q] = ~0ull;  // unmasked rows never rank
-        cthr += (mi[q] && ki[q] <= p.kthr) ? 1 : 0;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cthr += __shfl_xor_sync(0xffffffffu, cthr, o);
+    for (int q = 0; q < kSelRegRows; ++q) cthr += key[q] <= p.kthr ? 1 : 0;
+    cthr = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cthr)));
     const int kb = block_budget(p, n, cthr);
-    uint32_t commit = 0;  // bit q: row 32 q + lane is committed
+    uint32_t cbits = mbits;  // bit q: row 8 lane + q commits
+    if (n > kb && kb <= kSelRounds) {
+        unsigned long long sk[kSelRegRows];
+        int sq[kSelRegRows];
 #pragma unroll
-    for (int q = 0; q < kSelRegRows; ++q)
-        if (n <= kb && mi[q]) commit |= 1u << q;
-    if (n > kb) {
-        unsigned long long lk = 0;  // last chosen (key, row); row -1: none yet
-        int lr = -1;
+        for (int q = 0; q < kSelRegRows; ++q) {
+            sk[q] = key[q];
+            sq[q] = q;
+        }
+        // odd-even transposition sort of the lane's pairs
+#pragma unroll
+        for (int pass = 0; pass < kSelRegRows; ++pass) {
+#pragma unroll
+            for (int q = pass & 1; q + 1 < kSelRegRows; q += 2) {
+                if (key_row_less(sk[q + 1], sq[q + 1], sk[q], sq[q])) {
+                    const unsigned long long tk = sk[q];
+                    sk[q] = sk[q + 1];
+                    sk[q + 1] = tk;
+                    const int tq = sq[q];
+                    sq[q] = sq[q + 1];
+                    sq[q + 1] = tq;
+                }
+            }
+        }
+        cbits = 0;
         for (int round = 0; round < kb; ++round) {
-            unsigned long long bk = ~0ull;
-            int br = 0x7fffffff;
+            const unsigned hi = static_cast<unsigned>(sk[0] >> 32), lo = static_cast<unsigned>(sk[0]);
+            const unsigned m1 = __reduce_min_sync(0xffffffffu, hi);
+            const unsigned m2 = __reduce_min_sync(0xffffffffu, hi == m1 ? lo : 0xffffffffu);
+            const unsigned me = (hi == m1 && lo == m2) ? static_cast<unsigned>(lane) : 0xffffffffu;
+            if (static_cast<unsigned>(lane) == __reduce_min_sync(0xffffffffu, me)) {
+                cbits |= 1u << sq[0];
 #pragma unroll
-            for (int q = 0; q < kSelRegRows; ++q) {
-                const int j = q * 32 + lane;
-                const bool above = ki[q] > lk || (ki[q] == lk && j > lr);
-                const bool below = ki[q] < bk || (ki[q] == bk && j < br);
-                if (ki[q] != ~0ull && above && below) { bk = ki[q]; br = j; }
+                for (int q = 0; q + 1 < kSelRegRows; ++q) {
+                    sk[q] = sk[q + 1];
+                    sq[q] = sq[q + 1];
+                }
+                sk[kSelRegRows - 1] = ~0ull;
             }
+        }
+    } else if (n > kb) {
+        // smallest T with #(key <= T) >= kb; unselected rows (key ~0) never count
+        unsigned long long lo = 0, hi = ~0ull - 1;
+        while (lo < hi) {
+            const unsigned long long mid = lo + ((hi - lo) >> 1);
+            int c = 0;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const unsigned long long ok_ = __shfl_xor_sync(0xffffffffu, bk, o);
-                const int orow = __shfl_xor_sync(0xffffffffu, br, o);
-                if (ok_ < bk || (ok_ == bk && orow < br)) { bk = ok_; br = orow; }
-            }
-            if (br == 0x7fffffff) break;
-            if ((br & 31) == lane) commit |= 1u << (br >> 5);
-            lk = bk;
-            lr = br;
+            for (int q = 0; q < kSelRegRows; ++q) c += __popc(__ballot_sync(0xffffffffu, key[q] <= mid));
+            if (c >= kb) hi = mid;
+            else lo = mid + 1;
+        }
+        int clt = 0, before = 0;  // rows below T; rows at T in lower lanes
+        const uint32_t lower_lanes = (1u << lane) - 1u;
+#pragma unroll
+        for (int q = 0; q < kSelRegRows; ++q) {
+            clt += __popc(__ballot_sync(0xffffffffu, key[q] < lo));
+            before += __popc(__ballot_sync(0xffffffffu, key[q] == lo) & lower_lanes);
+        }
+        cbits = 0;
+#pragma unroll
+        for (int q = 0; q < kSelRegRows; ++q) {
+            const bool tie = key[q] == lo;
+            if (key[q] < lo || (tie && clt + before < kb)) cbits |= 1u << q;
+            before += tie ? 1 : 0;
         }
     }
 #pragma unroll
     for (int q = 0; q < kSelRegRows; ++q) {
-        const int i = q * 32 + lane;
-        if (mi[q]) {
-            const bool c = (commit >> q) & 1u;
-            if (c) p.tok[base + i] = ai[q];
-            p.masked_out[base + i] = c ? 0 : 1;
+        if ((mbits >> q) & 1u) {
+            const size_t i = base + lane * kSelRegRows + q;
+            const bool c = (cbits >> q) & 1u;
+            if (c) p.tok[i] = arg[q];
+            p.masked_out[i] = c ? 0 : 1;
         }
     }
 }
