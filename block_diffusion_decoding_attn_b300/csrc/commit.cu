@@ -552,11 +552,18 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 tc_fence_before();  // the row's TMEM loads (waited on) before the slot is freed
                 hi -= static_cast<unsigned>(ncol) * kMagic43Bits;
                 lo -= static_cast<unsigned>(ncol) * kMagic23Bits;
-                unsigned long long acc = (static_cast<unsigned long long>(hi) << 20) +
-                                         static_cast<long long>(static_cast<int>(lo));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc += shfl_xor64(acc, o);
-                __syncwarp();
+                // The warp's sum of (hi << 20) + lo with 32-bit warp reductions:
+                // per lane 0 <= hi < 2^28 and |lo| <= ncol * 2^19 <= 2^26, so
+                // 16-bit halves of hi and of lo + 2^26 sum over 32 lanes
+                // without overflow.
+                const unsigned lo_u = lo + (1u << 26);
+                const unsigned h0 = __reduce_add_sync(0xffffffffu, hi & 0xFFFFu);
+                const unsigned h1 = __reduce_add_sync(0xffffffffu, hi >> 16);
+                const unsigned l0 = __reduce_add_sync(0xffffffffu, lo_u & 0xFFFFu);
+                const unsigned l1 = __reduce_add_sync(0xffffffffu, lo_u >> 16);
+                const unsigned long long acc =
+                    (((static_cast<unsigned long long>(h1) << 16) + h0) << 20) +
+                    ((static_cast<unsigned long long>(l1) << 16) + l0) - (32ull << 26);
                 if (lane == 0) {
                     mbar_arrive(&sh.tfree[t]);  // this warp is done with the slot
                     sh.red_sum[q][pw] = acc;

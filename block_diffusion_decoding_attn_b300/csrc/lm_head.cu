@@ -21,7 +21,10 @@
 // its logits; with the maximum known, any chunk of a row can be summed on any
 // SM and the partial sums added with 64-bit integer atomics (the total does
 // not depend on the order). The work is (row, 8192-logit chunk) units in
-// row-major order, one contiguous range per CTA: a row's partial key stays in
+// row-major order, one contiguous range per CTA (one CTA per SM): a producer
+// warp streams the masked rows' chunks through a 3-slot shared-memory ring of
+// 64 KB bulk copies, 16 warps sum the terms (4 per scheduler, enough to keep
+// the FMA pipe fed; fewer or smaller chunks measured slower); a row's partial key stays in
 // registers until the row ends, then one atomic add; each CTA counts its units
 // of a block on the block's ticket once, and the CTA that completes the count
 // (L * chunks per row) ranks the block's masked rows and commits. Every row's
@@ -209,9 +212,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ---------------------------------------------------------------- commit given the row maximum
-constexpr int kTermThreads = 256;
-constexpr int kTermChunk = 8192;                        // logits per unit
-constexpr int kTermPer = kTermChunk / kTermThreads;     // 32 per thread
+constexpr int kTermConsumers = 512;                     // warps 1-16: the term sums
+constexpr int kTermThreads = 32 + kTermConsumers;       // warp 0: the producer
+constexpr int kTermChunk = 16384;                       // logits per unit (64 KB)
+constexpr int kTermSlots = 3;                           // ring depth
+constexpr int kTermPer = kTermChunk / kTermConsumers;   // 32 per consumer thread
+constexpr int kTermBarOff = kTermSlots * kTermChunk * 4;
+constexpr int kTermSmem = kTermBarOff + 2 * kTermSlots * 8 + 1024;
 
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* a, unsigned v) {
     unsigned old;
@@ -219,9 +226,20 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* a, unsigned v) {
     return old;
 }
 
-__global__ void __launch_bounds__(kTermThreads)
+// Barrier among the consumer warps only (id 1; 0 is __syncthreads).
+__device__ __forceinline__ void consumers_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kTermConsumers) : "memory");
+}
+
+__global__ void __launch_bounds__(kTermThreads, 1)
     commit_rowmax_kernel(const RowmaxCommitParams p) {
-    __shared__ unsigned long long s_part[kTermThreads / 32];
+    extern __shared__ uint8_t term_smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(term_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float* ring = reinterpret_cast<float*>(sm);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kTermBarOff);
+    uint64_t* empty = full + kTermSlots;
+    __shared__ unsigned long long s_part[kTermConsumers / 32];
     __shared__ int s_last;
     __shared__ unsigned long long s_key[sel::kSelChunk];
     __shared__ uint32_t s_mbits[kCommitMaxL / 32], s_cbits[kCommitMaxL / 32];
@@ -232,13 +250,66 @@ __global__ void __launch_bounds__(kTermThreads)
     // this CTA's contiguous range of units (row-major): a row's chunks follow
     // one another, so its partial key stays in registers until the row ends
     const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
+    const uint64_t limit = p.timeout_ns;
+    if (tid == 0) {
+        for (int i = 0; i < kTermSlots; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kTermConsumers / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
 
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        // Bulk copies of the masked rows' chunks (L2 evict-first) into the ring,
+        // in unit order; a row's mask is read here before its units are counted
+        // on the block's ticket by the consumers.
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int it = 0;
+            bool ok = true;
+            int r = static_cast<int>(u0 / nch), c = static_cast<int>(u0 % nch);
+            bool cur_masked = u0 < u1 && __ldcg(p.masked + r) != 0;
+            for (long long u = u0; u < u1 && ok; ++u, ++c) {
+                if (c == nch) {
+                    c = 0;
+                    ++r;
+                    cur_masked = __ldcg(p.masked + r) != 0;
+                }
+                if (!cur_masked) continue;
+                const int s = it % kTermSlots;
+                if (it >= kTermSlots && !mbar_wait(&empty[s], ((it / kTermSlots) - 1) & 1, limit)) {
+                    ok = false;
+                    break;
+                }
+                const int v0 = c * kTermChunk, n = min(kTermChunk, p.V - v0);
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(n) * 4);
+                bulk_load(ring + static_cast<size_t>(s) * kTermChunk,
+                          p.logits + static_cast<size_t>(r) * p.V + v0, static_cast<uint32_t>(n) * 4,
+                          &full[s], pol);
+                ++it;
+            }
+            if (!ok) atomicOr(p.status, kDevWaitTimeout);
+            // the copies issued last land before the CTA can exit
+            const uint64_t dl = drain_limit(limit);
+            for (int j = it - kTermSlots < 0 ? 0 : it - kTermSlots; j < it; ++j)
+                mbar_wait(&full[j % kTermSlots], (j / kTermSlots) & 1, dl);
+        }
+        __syncwarp();
+        return;
+    }
+
+    // -------------------------------------------------------------------- consumers
+    const int ct = tid - 32;  // consumer thread
+    const int cw = warp - 1;  // consumer warp
     int cur_r = -1, cur_b = -1;
-    bool cur_masked = false;
+    bool cur_masked = false, ok = true;
     key::f2 m2 = 0;
     unsigned hi = 0, lo = 0;
     int cnt = 0;
     unsigned bunits = 0;  // this CTA's units of block cur_b
+    int it = 0;
 
     // adds the CTA's partial key of row cur_r to key[cur_r]
     auto flush_row = [&]() {
@@ -249,15 +320,15 @@ __global__ void __launch_bounds__(kTermThreads)
                                  static_cast<long long>(static_cast<int>(lo));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) s_part[warp] = acc;
-        __syncthreads();
-        if (tid == 0) {
+        if (lane == 0) s_part[cw] = acc;
+        consumers_bar();
+        if (ct == 0) {
             unsigned long long tot = 0;
 #pragma unroll
-            for (int w = 0; w < kTermThreads / 32; ++w) tot += s_part[w];
+            for (int w = 0; w < kTermConsumers / 32; ++w) tot += s_part[w];
             atomicAdd(p.key + cur_r, tot);
         }
-        __syncthreads();
+        consumers_bar();
         hi = lo = 0;
         cnt = 0;
     };
@@ -265,14 +336,14 @@ __global__ void __launch_bounds__(kTermThreads)
     // block's count ranks it and commits
     auto flush_block = [&]() {
         if (cur_b < 0) return;
-        if (tid == 0) {
+        if (ct == 0) {
             __threadfence();  // this CTA's key additions before its ticket
             const unsigned t = atom_add_acq_rel(p.blk + cur_b, bunits);
             s_last = t + bunits == per_block;
             if (s_last) p.blk[cur_b] = 0;  // no other ticket of this call remains
         }
-        __syncthreads();
-        if (s_last && warp == 0) {
+        consumers_bar();
+        if (s_last && cw == 0) {
             __threadfence();
             const size_t base = static_cast<size_t>(cur_b) * p.L;
             int n = 0;
@@ -293,12 +364,16 @@ __global__ void __launch_bounds__(kTermThreads)
                 p.rowmax[base + i] = 0ull;
             }
         }
-        __syncthreads();
+        consumers_bar();
         bunits = 0;
     };
 
+    int r = static_cast<int>(u0 / nch), c = static_cast<int>(u0 % nch) - 1;
     for (long long u = u0; u < u1; ++u) {
-        const int r = static_cast<int>(u / nch), c = static_cast<int>(u % nch);
+        if (++c == nch) {
+            c = 0;
+            ++r;
+        }
         if (r != cur_r) {
             flush_row();
             const int b = r / p.L;
@@ -309,23 +384,25 @@ __global__ void __launch_bounds__(kTermThreads)
             cur_r = r;
             // the row's mask is read before this CTA counts it on the block's ticket
             cur_masked = __ldcg(p.masked + r) != 0;
-            if (!cur_masked && tid == 0 && c == 0) p.masked_out[r] = 0;  // the selection writes masked rows
+            if (!cur_masked && ct == 0 && c == 0) p.masked_out[r] = 0;  // the selection writes masked rows
             if (cur_masked) m2 = key::dup(key::dec_value(__ldcg(p.rowmax + r)));
         }
         ++bunits;
-        if (!cur_masked) continue;
-        const int v0 = c * kTermChunk;
-        const float* src = p.logits + static_cast<size_t>(r) * p.V + v0;
+        if (!cur_masked || !ok) continue;
+        const int s = it % kTermSlots;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (it / kTermSlots) & 1, limit));
+        ++it;
+        if (!ok) continue;  // keeps counting the units so that no ticket wait can hang
+        const int n = min(kTermChunk, p.V - c * kTermChunk);
+        const float4* src = reinterpret_cast<const float4*>(ring + static_cast<size_t>(s) * kTermChunk);
         float4 x[kTermPer / 4];
 #pragma unroll
-        for (int j = 0; j < kTermPer / 4; ++j) {
-            const int e = 4 * (j * kTermThreads + tid);
-            x[j] = v0 + e < p.V ? __ldcs(reinterpret_cast<const float4*>(src + e))
-                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        }
+        for (int j = 0; j < kTermPer / 4; ++j) x[j] = src[j * kTermConsumers + ct];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp has read its part of the slot
 #pragma unroll
         for (int j = 0; j < kTermPer / 4; ++j) {
-            if (v0 + 4 * (j * kTermThreads + tid) >= p.V) continue;
+            if (4 * (j * kTermConsumers + ct) >= n) continue;
             float d0, d1, d2, d3;
             key::upk(key::fsub2(key::pk(x[j].x, x[j].y), m2), d0, d1);
             key::upk(key::fsub2(key::pk(x[j].z, x[j].w), m2), d2, d3);
@@ -336,6 +413,7 @@ __global__ void __launch_bounds__(kTermThreads)
             cnt += 4;
         }
     }
+    if (!ok && ct == 0) atomicOr(p.status, kDevWaitTimeout);
     flush_row();
     flush_block();
 }
@@ -345,7 +423,10 @@ __global__ void __launch_bounds__(kTermThreads)
 size_t lm_head_smem_bytes() { return kGemmSmem; }
 
 cudaError_t configure_lm_head_kernels() {
-    return cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    const cudaError_t e =
+        cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(commit_rowmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTermSmem);
 }
 
 cudaError_t launch_lm_head(const CUtensorMap& a, const CUtensorMap& b, const LmHeadParams& p, int num_sms,
@@ -357,21 +438,10 @@ cudaError_t launch_lm_head(const CUtensorMap& a, const CUtensorMap& b, const LmH
 }
 
 cudaError_t launch_commit_rowmax(const RowmaxCommitParams& p, int num_sms, cudaStream_t s) {
-    // one wave: every CTA's range runs at once (the ranges are equal)
-    static int per_sm = 0;
-    if (per_sm == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, commit_rowmax_kernel, kTermThreads, 0) !=
-                cudaSuccess || n < 1) {
-            cudaGetLastError();
-            n = 1;
-        }
-        per_sm = n;
-    }
+    // one CTA per SM, every CTA's range at once (the ranges are equal)
     const long long units = static_cast<long long>(p.B) * p.L * ((p.V + kTermChunk - 1) / kTermChunk);
-    const long long cap = static_cast<long long>(num_sms) * per_sm;
-    const int grid = static_cast<int>(units < cap ? units : cap);
-    commit_rowmax_kernel<<<grid, kTermThreads, 0, s>>>(p);
+    const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+    commit_rowmax_kernel<<<grid, kTermThreads, kTermSmem, s>>>(p);
     return cudaGetLastError();
 }
 
