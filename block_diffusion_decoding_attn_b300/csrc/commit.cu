@@ -262,6 +262,51 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
                 }
         }
     }
+    __syncthreads();  // the cluster's share (sh.total, sh.row0) is known
+    // The producer (lane 0 of its warp): the cluster's masked rows go through
+    // the ring in row order, max(nchunks, 1) entries each; the unmasked ones
+    // are only marked in masked_out. It issues the first row's entries before
+    // the cluster barrier (they use only this CTA's barriers) and the rest once
+    // the first entry has landed, so that the first row arrives first.
+    const uint64_t pol = l2_policy_evict_first();
+    const int per_row = max(nchunks, 1);
+    int pr_it = 0, pr_done = 0, pr_r = sh.row0, pr_c = 0;  // entries issued; rows started; row; chunk
+    bool pr_ok = true;
+    auto produce = [&](int it_end) {
+        while (pr_ok && pr_it < it_end) {
+            if (pr_c == 0) {
+                // next masked row of the share; masked may alias masked_out:
+                // this read precedes the block's selection, which waits for
+                // this row's ticket
+                while (pr_r < rows && __ldcg(p.masked + pr_r) == 0) {
+                    if (rank == 0) p.masked_out[pr_r] = 0;
+                    ++pr_r;
+                }
+                if (pr_r >= rows || pr_done == sh.total) return;  // the next cluster's first row
+                ++pr_done;
+            }
+            const int s = pr_it % kSlots;
+            if (pr_it >= kSlots && !mbar_wait(&sh.empty[s], ((pr_it / kSlots) - 1) & 1, limit)) {
+                pr_ok = false;
+                return;
+            }
+            const int lo = pr_c * kChunk, n = min(kChunk, cnt - lo);
+            if (n > 0) {
+                mbar_arrive_expect_tx(&sh.full[s], static_cast<uint32_t>(n) * 4);
+                bulk_load(ring + static_cast<size_t>(s) * kChunk,
+                          p.logits + static_cast<size_t>(pr_r) * p.V + v0 + lo, static_cast<uint32_t>(n) * 4,
+                          &sh.full[s], pol);
+            } else {
+                mbar_arrive(&sh.full[s]);
+            }
+            ++pr_it;
+            if (++pr_c == per_row) {
+                pr_c = 0;
+                ++pr_r;
+            }
+        }
+    };
+    if (warp == kProducerWarp && lane == 0) produce(per_row);
     tc_fence_before();
     // Every CTA's barriers are initialised before any remote arrival.
     cluster_sync_all();
@@ -269,53 +314,21 @@ __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kThread
     // The cluster's scans are over. When masked_out is the masked buffer, no
     // block selection writes the mask before every cluster has scanned it (the
     // selecting warp waits for this count to reach the number of clusters).
-    if (rank == 0 && tid == 0) red_add_release_gpu(p.counters + kCtrStarted, 1u);
+    // (Counted by a warp that is idle until the first row's exchange.)
+    if (rank == 0 && warp == kSumSenderWarp && lane == 0) red_add_release_gpu(p.counters + kCtrStarted, 1u);
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------------- producer
-        // The masked rows of this cluster go through the ring in row order,
-        // max(nchunks, 1) entries each; the unmasked ones are only marked in
-        // masked_out.
         if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            const int per_row = max(nchunks, 1);
-            int it = 0;  // ring entries issued
-            bool ok = true;
-            const int total = sh.total;
-            int done = 0;
-            for (int r = sh.row0; r < rows && ok; ++r) {
-                // masked may alias masked_out: this read precedes the block's
-                // selection, which waits for this row's ticket.
-                if (__ldcg(p.masked + r) == 0) {
-                    if (rank == 0) p.masked_out[r] = 0;
-                    continue;
-                }
-                if (done == total) break;  // the next cluster's first row
-                ++done;
-                for (int c = 0; c < per_row; ++c, ++it) {
-                    const int s = it % kSlots;
-                    if (it >= kSlots && !mbar_wait(&sh.empty[s], ((it / kSlots) - 1) & 1, limit)) {
-                        ok = false;
-                        break;
-                    }
-                    const int lo = c * kChunk, n = min(kChunk, cnt - lo);
-                    if (n > 0) {
-                        mbar_arrive_expect_tx(&sh.full[s], static_cast<uint32_t>(n) * 4);
-                        bulk_load(ring + static_cast<size_t>(s) * kChunk,
-                                  p.logits + static_cast<size_t>(r) * p.V + v0 + lo,
-                                  static_cast<uint32_t>(n) * 4, &sh.full[s], pol);
-                    } else {
-                        mbar_arrive(&sh.full[s]);
-                    }
-                }
-            }
-            if (!ok) atomicOr(p.status, kDevWaitTimeout);
+            if (pr_it > 0 && !mbar_wait(&sh.full[0], 0, limit)) pr_ok = false;
+            produce(0x7fffffff);
+            if (!pr_ok) atomicOr(p.status, kDevWaitTimeout);
             // Let the copies already issued land before the CTA can exit (an
             // entry is issued only once the one kSlots before it was consumed, so
             // at most the last kSlots can be in flight; after a normal run they
             // have all landed). Also when a consumer gave up instead.
             const uint64_t dl = drain_limit(limit);
-            for (int j = it - kSlots < 0 ? 0 : it - kSlots; j < it; ++j)
+            for (int j = pr_it - kSlots < 0 ? 0 : pr_it - kSlots; j < pr_it; ++j)
                 mbar_wait(&sh.full[j % kSlots], (j / kSlots) & 1, dl);
         }
         __syncwarp();
