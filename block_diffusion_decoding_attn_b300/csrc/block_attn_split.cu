@@ -68,7 +68,16 @@ __global__ void __launch_bounds__(320, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pair = blockIdx.x % p.n_pairs;
     const int split = blockIdx.x / p.n_pairs;
-    const int kvh = blockIdx.y, b = blockIdx.z;
+    const int kvh = blockIdx.y;
+    int b = blockIdx.z;
+    if (p.ctx_group) {
+        // Training layout: block j of a sequence sees j * L cache keys, so the
+        // grid takes block j of every sequence for j descending (longest
+        // first), which keeps the last wave short.
+        const int nseq = static_cast<int>(gridDim.z) / p.ctx_group;
+        const int j = p.ctx_group - 1 - static_cast<int>(blockIdx.z) / nseq;
+        b = static_cast<int>(blockIdx.z) % nseq * p.ctx_group + j;
+    }
 
     int C = p.ctx_group ? (b % p.ctx_group) * p.L : p.ctx_len[b];
     if (C < 0 || C > p.ctx_cap) {
