@@ -635,18 +635,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             for (int j = 0; j < n && ok; ++j, ++gt) {
                 const int lv = 2 * gt + 1, lk = 2 * gt + 2;
-                // ---- tile A
-                if (!mbar_wait(&p_full[0], gt & 1, limit) || !wait_slot(lv)) { ok = false; break; }
+                const bool more = j + 1 < n;
+                // ---- tile A: every input of its group (P_A, V_j, K_j+1) is in
+                // before the first of its MMAs, so that P V and the next QK^T
+                // go to the tensor core back to back
+                if (!mbar_wait(&p_full[0], gt & 1, limit) || !wait_slot(lv) || (more && !wait_slot(lk))) {
+                    ok = false;
+                    break;
+                }
                 // the previous unit's O_A has been read out before it is overwritten
                 if (j == 0 && nit > 0 && !mbar_wait(&o_empty[0], (nit - 1) & 1, limit)) { ok = false; break; }
                 zero_tail(kv_tile(it.t0 + j, nc, it.C, p.L), lv);
                 tc_fence_after();
-                if (lane == 0) issue_pv(0, lv, j == 0);
-                __syncwarp();
-                const bool more = j + 1 < n;
-                if (more && !wait_slot(lk)) { ok = false; break; }
-                tc_fence_after();
                 if (lane == 0) {
+                    issue_pv(0, lv, j == 0);
                     if (more) {
                         issue_s(0, lk);
                         tc_commit(&s_full[0]);
@@ -717,17 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         #pragma unroll
                     for (int c = 0; c < kTile; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
                 }
-                // row max: four independent chains of 3-input max over s[4..123],
-                // the last four columns on two of them, then combined
-                float m4[4] = {s[0], s[1], s[2], s[3]};
-        #pragma unroll
-                for (int c = 4; c + 8 <= kTile; c += 8) {
-        #pragma unroll
-                    for (int q = 0; q < 4; ++q) m4[q] = max3f(m4[q], s[c + 2 * q], s[c + 2 * q + 1]);
-                }
-                m4[0] = max3f(m4[0], s[kTile - 4], s[kTile - 3]);
-                m4[1] = max3f(m4[1], s[kTile - 2], s[kTile - 1]);
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                const float mx = row_max128(s);
                 const float m_tile = mx * sl2;
                 if (j == 0) {
                     m_run = m_tile;

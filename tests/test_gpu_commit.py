@@ -120,6 +120,57 @@ def test_ties_and_alias(tt, oracle_lib):
     _check_step(tt, oracle_lib, lg, 2, 40, masked, 6, tok, alias=True)
 
 
+@pytest.mark.parametrize("L,k", [(256, 1), (256, 8), (256, 95), (256, 96), (256, 97),
+                                 (256, 128), (256, 200), (256, 229), (200, 7), (200, 150),
+                                 (33, 20)])
+def test_selection_budgets_and_key_ties(tt, oracle_lib, L, k):
+    # Blocks of up to 256 rows: budgets up to 96 take the per-round warp
+    # minimum, larger ones the binary search on the key. Identical logit rows
+    # give identical keys in different lanes and in one lane (rows 8 apart
+    # and adjacent), some of them at the cut of the budget; the lower row wins.
+    w = wl.custom("sel", 2, L, 1, 1, 8, 8, (0, 0), V=2048, k=k)
+    lg = wl.logits(w, seed=21)
+    seen = set()
+    groups = []
+    for g in ([3, 11, 100, L - 1], [40, 41, 42, 43, 44], [7, 200, 129]):
+        g = [r % L for r in g if r % L not in seen]
+        seen.update(g)
+        groups.append(g)
+    for b in range(2):
+        for g in groups:
+            for r in g[1:]:
+                lg[b * L + r] = lg[b * L + g[0]]
+    masked = wl.random_mask(w, 0.9, seed=8)
+    masked[[3, L + groups[1][0]]] = 1
+    tok = np.full(w.rows, -1, np.int32)
+    _check_step(tt, oracle_lib, lg, 2, L, masked, k, tok)
+
+
+@pytest.mark.parametrize("rank", [0, 30, 120, 180])
+def test_selection_cut_inside_a_key_tie(tt, oracle_lib, rank):
+    # The row at confidence rank `rank` of block 0 is copied to four rows in
+    # different lanes and one lane (rows 8 apart and adjacent); the budget
+    # ends in the middle of that tie (the per-round path below 96 commits, the
+    # binary search above), so the lower rows of the tie commit.
+    L, V = 256, 2048
+    w = wl.custom("cut", 2, L, 1, 1, 8, 8, (0, 0), V=V, k=1)
+    lg = wl.logits(w, seed=23)
+    masked = wl.random_mask(w, 0.9, seed=9)
+    masked[:L][[5, 6, 13, 77, 160]] = 1
+    _, _, keys, _ = oracle_lib.commit(lg, 2, L, masked, 1, np.full(w.rows, -1, np.int32))
+    cand = [r for r in np.argsort(keys[:L], kind="stable") if masked[r] and r not in (5, 6, 13, 77, 160)]
+    src = cand[rank]
+    for r in (5, 6, 13, 77, 160):
+        lg[r] = lg[src]
+    k = rank + 3  # the tie spans ranks rank .. rank + 5 (with src): cut after three
+    tok = np.full(w.rows, -1, np.int32)
+    _, om = _check_step(tt, oracle_lib, lg, 2, L, masked, k, tok)
+    tie = sorted([5, 6, 13, 77, 160, int(src)])
+    committed = [r for r in tie if om[r] == 0]
+    assert 0 < len(committed) < len(tie)
+    assert committed == tie[:len(committed)]
+
+
 @pytest.mark.parametrize("name", ["b8_c4096_l32", "b16_c1024_l256", "b4_gen8k_32x256",
                                   "b64_ragged8k32k_l64"])
 def test_full_workloads_first_step(tt, oracle_lib, name):
