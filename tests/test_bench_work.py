@@ -63,3 +63,34 @@ def test_byte_counts():
     assert b.append_bytes(w) == 2 * blk                        # block read again, cache rows written
     masked = 6
     assert b.commit_bytes(w, masked) == masked * w.V * 4 + 2 * w.rows + 4 * min(w.k, w.L) * w.B
+
+
+def test_profiled_traffic_entries_and_source_keys(tmp_path, monkeypatch):
+    # Every traffic entry names an existing ncu summary and existing kernel
+    # sources; the bench reports the DRAM bytes only while those sources hash
+    # to the captured value (an edited kernel reports null).
+    import json
+    b = _bench()
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        t = json.load(f)
+    assert t
+    for kernel, entries in t.items():
+        for workload, e in entries.items():
+            assert os.path.exists(os.path.join(ROOT, e["capture"])), e["capture"]
+            assert all(os.path.exists(os.path.join(ROOT, s)) for s in e["sources"])
+            assert e["dram_bytes_per_launch"] > 0
+            got = b.profiled_traffic(kernel, workload)
+            assert got in (None, e["dram_bytes_per_launch"])
+    # a changed source voids the entry
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    entry = {"dram_bytes_per_launch": 123, "sources": ["k.cu"], "capture": "x.md",
+             "sources_sha256": b.sources_hash(["k.cu"])}
+    (prof / "traffic.json").write_text(json.dumps({"attn": {"w": entry}}))
+    assert b.profiled_traffic("attn", "w") == 123
+    src.write_text("kernel v2")
+    assert b.profiled_traffic("attn", "w") is None
+    assert b.profiled_traffic("attn", "other") is None
