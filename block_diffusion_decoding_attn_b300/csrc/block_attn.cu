@@ -636,15 +636,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < n && ok; ++j, ++gt) {
                 const int lv = 2 * gt + 1, lk = 2 * gt + 2;
                 const bool more = j + 1 < n;
-                // ---- tile A: every input of its group (P_A, V_j, K_j+1) is in
-                // before the first of its MMAs, so that P V and the next QK^T
-                // go to the tensor core back to back
-                if (!mbar_wait(&p_full[0], gt & 1, limit) || !wait_slot(lv) || (more && !wait_slot(lk))) {
+                // ---- tile A: P_A complete also means V_j and K_j+1 have landed
+                // (tile A's softmax waits for them before it signals) and, on a
+                // unit's first tile, that the previous unit's O_A has been read
+                // out (each softmax thread signals that first); one wait, so
+                // that the group follows the previous one without a gap
+                if (!mbar_wait(&p_full[0], gt & 1, limit)) {
                     ok = false;
                     break;
                 }
-                // the previous unit's O_A has been read out before it is overwritten
-                if (j == 0 && nit > 0 && !mbar_wait(&o_empty[0], (nit - 1) & 1, limit)) { ok = false; break; }
                 zero_tail(kv_tile(it.t0 + j, nc, it.C, p.L), lv);
                 tc_fence_after();
                 if (lane == 0) {
@@ -657,9 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncwarp();
-                // ---- tile B
+                // ---- tile B (its inputs are tile A's, already in)
                 if (!mbar_wait(&p_full[1], gt & 1, limit)) { ok = false; break; }
-                if (j == 0 && nit > 0 && !mbar_wait(&o_empty[1], (nit - 1) & 1, limit)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
                     issue_pv(1, lv, j == 0);
@@ -759,6 +758,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(ts + h * 32, pk);  // P over the first 64 columns of S_X
                 }
                 l_run += ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
+                if (x == 0 && row == 0) {
+                    // the MMA group this P starts reads V_j and K_j+1: have them in first
+                    const int lv = 2 * gt + 1, lk = lv + 1;
+                    if (!mbar_wait(&full[lv % kRing], (lv / kRing) & 1, limit) ||
+                        (j + 1 < n && !mbar_wait(&full[lk % kRing], (lk / kRing) & 1, limit)))
+                        atomicOr(p.status, kDevWaitTimeout);
+                }
                 tc_fence_before();
                 mbar_arrive(&p_full[x]);
             }
