@@ -50,8 +50,11 @@
 // it computes tile B's P V and next S, and the other way round. tcgen05.mma
 // operations complete in issue order, so "S_X(j) complete" also means
 // "P V of tile X for KV tile j-1 complete": the softmax may then overwrite S_X
-// with P and rescale O_X without another wait. A unit's first P V into O_X
-// waits until the softmax warps have read the previous unit's O_X.
+// with P and rescale O_X without another wait. The MMA warp waits on one
+// barrier per group: P_X complete also means the group's V_j and K_j+1 have
+// landed (tile A's softmax waits for them before it signals) and, on a unit's
+// first tile, that the previous unit's O_X has been read out (each softmax
+// thread signals that before it can signal the next unit's P).
 #include "ptx.cuh"
 #include "tt_internal.h"
 
