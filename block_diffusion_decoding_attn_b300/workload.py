@@ -270,3 +270,40 @@ def lm_head_inputs(M: int, K: int, V: int, seed: int = 0, wid: int = 200, step: 
     hid = _fill_normal(M * K, 1.0, seed, wid, _T_HIDDEN + 16 * step, True).reshape(M, K)
     w = _fill_normal(V * K, 2.0 / math.sqrt(K), seed, wid, _T_WEIGHT, True).reshape(V, K)
     return hid, w
+
+
+def _fill_int(n: int, lo: int, hi: int, scale: float, seed: int, wid: int, tid: int) -> np.ndarray:
+    """n uniform integers in [lo, hi] times `scale` (a power of two), chunk-keyed,
+    as bf16 bit patterns (exact: |integer| <= 256)."""
+    out = np.empty(n, dtype=np.uint16)
+    nchunks = max(1, -(-n // _CHUNK))
+
+    def work(c):
+        a, b = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        v = _rng(seed, wid, tid, c).integers(lo, hi + 1, size=b - a).astype(np.float32)
+        out[a:b] = to_bf16_bits(v * np.float32(scale))
+
+    if nchunks == 1:
+        work(0)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(work, range(nchunks)))
+    return out
+
+
+def lm_head_exact_inputs(M: int, K: int, V: int, seed: int = 0, wid: int = 201, step: int = 0):
+    """LM head inputs whose logits are exact in fp32 whatever the summation order:
+    hidden [M][K] = i / 8 and weight [V][K] = j * 2^e with i, j uniform in
+    [-8, 8] and 2^e the power of two nearest 2 / (3 sqrt K), so the logits have
+    variance 9 K 2^(2e), between 1 and 16. Every product is a multiple of
+    u = 2^(e-3) and every partial sum is at most 64 K u in magnitude, an integer
+    count of u below 2^24 for K < 2^18: fp32 holds each one exactly, so an fp32
+    accumulation in any order equals the exact sum (the logits of both the fp64
+    LM head and the tensor-core one). Small integers also make ties among the
+    logits and among the rows' confidences common."""
+    if not 0 < K < 1 << 18:
+        raise ValueError("lm_head_exact_inputs: K must be in [1, 2^18)")
+    e = round(math.log2(2.0 / (3.0 * math.sqrt(K))))
+    hid = _fill_int(M * K, -8, 8, 0.125, seed, wid, _T_HIDDEN + 16 * step).reshape(M, K)
+    w = _fill_int(V * K, -8, 8, 2.0 ** e, seed, wid, _T_WEIGHT).reshape(V, K)
+    return hid, w

@@ -44,3 +44,27 @@ def test_rows_subset_and_widening(oracle_lib):
     np.testing.assert_array_equal(oracle_lib.lm_head(hid, w, rows=[4, 1]), full[[4, 1]])
     x = np.float32([1.0, -2.5, 3.140625, 0.0])
     assert np.array_equal(oracle_lib.bf16_to_f64(wl.to_bf16_bits(x)), x.astype(np.float64))
+
+
+def test_exact_inputs_give_fp32_exact_logits(oracle_lib):
+    # The integer-valued inputs' logits are exact in fp32 in any summation
+    # order: the fp64 logits round-trip through fp32, and fp32 sums taken
+    # forwards, backwards and pairwise (numpy's blocked sum) all equal them.
+    for K in (8, 136, 2688):
+        hid, w = wl.lm_head_exact_inputs(5, K, 7, seed=K)
+        ref = oracle_lib.lm_head(hid, w)
+        assert np.array_equal(ref.astype(np.float32).astype(np.float64), ref)
+        h = wl.bf16_bits_to_f32(hid)
+        ww = wl.bf16_bits_to_f32(w)
+        prod = h[:, None, :] * ww[None, :, :]           # exact products, fp32
+        fwd = np.zeros(ref.shape, np.float32)
+        bwd = np.zeros(ref.shape, np.float32)
+        for k in range(K):
+            fwd += prod[:, :, k]
+            bwd += prod[:, :, K - 1 - k]
+        np.testing.assert_array_equal(fwd, ref)
+        np.testing.assert_array_equal(bwd, ref)
+        np.testing.assert_array_equal(prod.sum(axis=2, dtype=np.float32), ref)
+        # values on the stated grid, logits neither all zero nor overflowing
+        assert set(np.unique(h * 8).astype(int)) <= set(range(-8, 9))
+        assert 0.5 < ref.std() < 5.0
