@@ -33,6 +33,7 @@ LIB_PATH = os.path.join(_HERE, "libtt.so")
 TT_OK = 0
 TT_ERR_INVALID_ARG, TT_ERR_UNSUPPORTED, TT_ERR_CUDA, TT_ERR_TIMEOUT, TT_ERR_DEVICE_CHECK = (
     -1, -2, -3, -4, -5)
+TT_ERR_NOT_READY = -6
 TT_DEV_CTX_LEN_RANGE = 1
 TT_DEV_WAIT_TIMEOUT = 2
 
@@ -62,6 +63,7 @@ def lib() -> ctypes.CDLL:
             L.tt_create.argtypes = [ctypes.POINTER(P), I]
             L.tt_destroy.argtypes = [P]
             L.tt_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+            L.tt_sync.argtypes = [P, P, ctypes.c_uint, ctypes.POINTER(ctypes.c_int)]
             L.tt_set_wait_timeout.argtypes = [P, ctypes.c_ulonglong]
             L.tt_set_attn_schedule.argtypes = [P, I, I, I, I]
             L.tt_reserve.argtypes = [P, ctypes.POINTER(AttnDesc), I, I]
@@ -129,6 +131,22 @@ class Handle:
         if rc not in (TT_OK, TT_ERR_TIMEOUT, TT_ERR_DEVICE_CHECK):
             _check(rc, "tt_get_error")
         return st.value
+
+    def sync(self, stream=None, timeout_ms: int = 1000):
+        """Waits on the host for at most timeout_ms for the work issued on
+        `stream` (default: the current torch stream of the handle's device) to
+        finish (tt_sync). Returns (done, status): done False if it was still
+        running; status = the TT_DEV_* bits, not cleared."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        st = ctypes.c_int(0)
+        rc = lib().tt_sync(self._h, ctypes.c_void_p(stream.cuda_stream), int(timeout_ms),
+                           ctypes.byref(st))
+        if rc == TT_ERR_NOT_READY:
+            return False, 0
+        _check(rc, "tt_sync")
+        return True, st.value
 
     def set_wait_timeout(self, ns: int):
         _check(lib().tt_set_wait_timeout(self._h, int(ns)), "tt_set_wait_timeout")

@@ -12,6 +12,7 @@
 // streams, other host threads) race on it and must be ordered by the caller.
 #include <mutex>
 
+#include "host_trace.h"
 #include "tt.h"
 #include "tt_internal.h"
 
@@ -44,6 +45,7 @@ int fail(int status, const char* msg) {
 
 extern "C" int tt_commit_noalloc(const float* logits, int B, int L, int V, const uint8_t* masked,
                                  int k, int32_t* tok, uint8_t* masked_out, void* stream) {
+    tt::TraceRange tr("tt_commit_noalloc");
     if (B < 0 || L < 1 || k < 1) return fail(TT_ERR_INVALID_ARG, "needs B >= 0, L >= 1, k >= 1");
     if (static_cast<long>(B) * L > kMaxRows || B > kMaxBlocks)
         return fail(TT_ERR_UNSUPPORTED,

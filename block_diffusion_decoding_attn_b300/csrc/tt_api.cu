@@ -2,13 +2,16 @@
 // encoding and kernel launches. See include/tt.h for the contract.
 #include <cudaTypedefs.h>
 
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <thread>
 
+#include "host_trace.h"
 #include "tt.h"
 #include "tt_internal.h"
 
@@ -313,6 +316,7 @@ const char* tt_status_string(int s) {
         case TT_ERR_CUDA: return "TT_ERR_CUDA";
         case TT_ERR_TIMEOUT: return "TT_ERR_TIMEOUT";
         case TT_ERR_DEVICE_CHECK: return "TT_ERR_DEVICE_CHECK";
+        case TT_ERR_NOT_READY: return "TT_ERR_NOT_READY";
         default: return "TT_ERR_UNKNOWN";
     }
 }
@@ -448,6 +452,29 @@ int tt_get_error(tt_handle h, int* device_status) {
     return v ? TT_ERR_DEVICE_CHECK : TT_OK;
 }
 
+int tt_sync(tt_handle h, void* stream, unsigned timeout_ms, int* device_status) {
+    if (device_status) *device_status = 0;
+    if (!h) return fail(TT_ERR_INVALID_ARG, "tt_sync: handle is NULL");
+    DeviceGuard g(h->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        const cudaError_t e = cudaStreamQuery(s);
+        if (e == cudaSuccess) break;
+        if (e != cudaErrorNotReady) return cuda_fail(e, "tt_sync: cudaStreamQuery");
+        if (std::chrono::steady_clock::now() - t0 >= std::chrono::milliseconds(timeout_ms))
+            return fail(TT_ERR_NOT_READY, "tt_sync: the stream is still busy after %u ms", timeout_ms);
+        std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+    // The stream has drained: this copy waits for nothing else on it.
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, h->status, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "tt_sync: read status");
+    if (device_status) *device_status = static_cast<int>(v);
+    return TT_OK;
+}
+
 }  // extern "C"
 
 // Body of tt_block_attn (causal = 0), tt_block_attn_causal (causal = 1) and
@@ -568,18 +595,21 @@ extern "C" {
 int tt_block_attn(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
                   const void* v_blk, const void* k_ctx, const void* v_ctx,
                   const int32_t* ctx_len, void* out, void* stream) {
+    tt::TraceRange tr("tt_block_attn");
     return block_attn_call(h, d, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out, stream, 0);
 }
 
 int tt_block_attn_causal(tt_handle h, const tt_attn_desc* d, const void* q, const void* k_blk,
                          const void* v_blk, const void* k_ctx, const void* v_ctx,
                          const int32_t* ctx_len, void* out, void* stream) {
+    tt::TraceRange tr("tt_block_attn_causal");
     return block_attn_call(h, d, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, out, stream, 1);
 }
 
 int tt_block_attn_train(tt_handle h, const tt_train_desc* t, const void* q, const void* k_noisy,
                         const void* v_noisy, const void* k_clean, const void* v_clean, void* out,
                         void* stream) {
+    tt::TraceRange tr("tt_block_attn_train");
     if (!h) return fail(TT_ERR_INVALID_ARG, "tt_block_attn_train: handle is NULL");
     tt_attn_desc d;
     const int st = train_desc(t, &d);
@@ -591,6 +621,7 @@ int tt_block_attn_train(tt_handle h, const tt_train_desc* t, const void* q, cons
 
 int tt_kv_append(tt_handle h, const tt_attn_desc* d, const void* k_blk, const void* v_blk,
                  void* k_ctx, void* v_ctx, int32_t* ctx_len, void* stream) {
+    tt::TraceRange tr("tt_kv_append");
     if (!h) return fail(TT_ERR_INVALID_ARG, "tt_kv_append: handle is NULL");
     if (!d) return fail(TT_ERR_INVALID_ARG, "tt_kv_append: desc is NULL");
     if (d->B < 0 || d->B > 65535) return fail(TT_ERR_INVALID_ARG, "B=%d outside [0, 65535]", d->B);
@@ -717,6 +748,7 @@ extern "C" {
 
 int tt_commit(tt_handle h, const float* logits, int B, int L, int V, const uint8_t* masked, int k,
               int32_t* tok, uint8_t* masked_out, void* stream) {
+    tt::TraceRange tr("tt_commit");
     if (k < 1) return fail(TT_ERR_INVALID_ARG, "tt_commit: k=%d < 1", k);
     return commit_impl(h, "tt_commit", logits, B, L, V, masked, k, 0, 0ull, tok, masked_out, stream);
 }
@@ -724,6 +756,7 @@ int tt_commit(tt_handle h, const float* logits, int B, int L, int V, const uint8
 int tt_commit_threshold(tt_handle h, const float* logits, int B, int L, int V,
                         const uint8_t* masked, double gamma, int steps_left, int32_t* tok,
                         uint8_t* masked_out, void* stream) {
+    tt::TraceRange tr("tt_commit_threshold");
     if (steps_left < 1)
         return fail(TT_ERR_INVALID_ARG, "tt_commit_threshold: steps_left=%d < 1", steps_left);
     if (std::isnan(gamma)) return fail(TT_ERR_INVALID_ARG, "tt_commit_threshold: gamma is NaN");
@@ -774,6 +807,7 @@ extern "C" {
 
 int tt_lm_head(tt_handle h, const void* hidden, const void* weight, int M, int K, int V, float* logits,
                void* stream) {
+    tt::TraceRange tr("tt_lm_head");
     if (!h) return fail(TT_ERR_INVALID_ARG, "tt_lm_head: handle is NULL");
     if (M < 0 || K < 8 || K % 8 || V < 4 || V % 4)
         return fail(TT_ERR_INVALID_ARG, "tt_lm_head: needs M >= 0, K >= 8 with K %% 8 == 0, V >= 4 with V %% 4 == 0");
@@ -851,6 +885,7 @@ static int commit_rowmax_impl(tt_handle h, const char* name, const float* logits
 
 int tt_commit_rowmax(tt_handle h, const float* logits, int B, int L, int V, const uint8_t* masked, int k,
                      int32_t* tok, uint8_t* masked_out, void* stream) {
+    tt::TraceRange tr("tt_commit_rowmax");
     if (k < 1) return fail(TT_ERR_INVALID_ARG, "tt_commit_rowmax: k=%d < 1", k);
     return commit_rowmax_impl(h, "tt_commit_rowmax", logits, B, L, V, masked, k, 0, 0ull, tok, masked_out,
                               stream);

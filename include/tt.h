@@ -45,7 +45,8 @@ typedef enum {
     TT_ERR_UNSUPPORTED = -2,  /* a shape outside the supported set (see below)          */
     TT_ERR_CUDA = -3,         /* a CUDA runtime or driver call failed                   */
     TT_ERR_TIMEOUT = -4,      /* tt_get_error: a bounded wait in a kernel gave up       */
-    TT_ERR_DEVICE_CHECK = -5  /* tt_get_error: a kernel's argument check failed (ctx_len) */
+    TT_ERR_DEVICE_CHECK = -5, /* tt_get_error: a kernel's argument check failed (ctx_len) */
+    TT_ERR_NOT_READY = -6     /* tt_sync: the stream's work had not finished in time    */
 } tt_status;
 
 /* Bits of the device status word (tt_get_error). */
@@ -85,6 +86,19 @@ int tt_reserve(tt_handle handle, const tt_attn_desc* attn, int commit_B, int com
  * TT_ERR_TIMEOUT if a wait timed out, TT_ERR_DEVICE_CHECK if only an argument
  * check failed, TT_ERR_CUDA if the synchronization reported a CUDA error. */
 int tt_get_error(tt_handle handle, int* device_status);
+
+/* Waits on the host, for at most timeout_ms milliseconds, until the work
+ * issued so far on `stream` (a cudaStream_t as void*, NULL = legacy default
+ * stream) has finished, polling cudaStreamQuery; neither the device nor other
+ * streams are synchronized, and nothing is cancelled. Returns TT_OK once the
+ * stream has drained, with *device_status (may be NULL) = the TT_DEV_* bits of
+ * the handle's status word, read but not cleared (tt_get_error clears them);
+ * TT_ERR_NOT_READY if the work is still running after timeout_ms (it runs on:
+ * call again, or tt_get_error); TT_ERR_CUDA if the stream reported an error.
+ * timeout_ms = 0 looks once. A host-side watchdog for a serving loop: a call
+ * whose kernels gave up a pipeline wait finishes within the handle's wait
+ * limit (tt_set_wait_timeout) and shows TT_DEV_WAIT_TIMEOUT here. */
+int tt_sync(tt_handle handle, void* stream, unsigned timeout_ms, int* device_status);
 
 /* Sets how long a pipeline wait inside a kernel may last before it gives up,
  * sets TT_DEV_WAIT_TIMEOUT and lets the kernel wind down (default 1 s). */

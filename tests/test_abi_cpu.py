@@ -49,6 +49,8 @@ def test_host_argument_errors(tt):
     assert lib.tt_set_attn_schedule(None, 0, 0, 0, 0) == -1
     assert lib.tt_commit_keys(None, None, None, 1, None) == -1
     assert lib.tt_get_error(None, None) == -1
+    assert lib.tt_status_string(-6) == b"TT_ERR_NOT_READY"
+    assert lib.tt_sync(None, None, 0, None) == -1 and b"tt_sync" in lib.tt_last_error()
     # the context-tower update and the training layout check the handle first too
     assert lib.tt_block_attn_causal(None, ctypes.byref(d), *([None] * 7), None) == -1
     assert lib.tt_kv_append(None, ctypes.byref(d), *([None] * 5), None) == -1

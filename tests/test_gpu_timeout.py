@@ -7,7 +7,14 @@ sets TT_DEV_WAIT_TIMEOUT, lets the work it issued itself finish (TMA copies,
 MMAs and exchange messages, under a separate long bound) and returns. The next
 call with the normal limit must then give the oracle's result. Nothing here
 traps, faults or hangs: the failure is a wait limit that nothing can meet.
+
+The host-side watchdog tt_sync polls a stream for a bounded time: a stream
+kept busy by a bounded spin (torch.cuda._sleep) is reported as still running
+within the poll limit, and a commit whose waits gave up shows the status bit
+there without clearing it.
 """
+import time
+
 import numpy as np
 import pytest
 
@@ -82,3 +89,41 @@ def test_attention_timeout_reported_then_exact(tt, oracle_lib):
                                 rows=rows)
     got = out.float().cpu().numpy().astype(np.float64)[rows[:, 0], rows[:, 1], rows[:, 2]]
     assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
+
+
+def test_sync_is_bounded_and_reports_without_clearing(tt, oracle_lib):
+    import torch
+    h = tt.handle(0)
+    assert h.get_error() == 0
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(1 << 31)  # a bounded spin of 2^31 clocks, about a second
+    t0 = time.monotonic()
+    done, _ = h.sync(stream=s, timeout_ms=5)
+    assert not done and time.monotonic() - t0 < 0.5
+    done, st = h.sync(stream=s, timeout_ms=60000)
+    assert done and st == 0
+    # a commit whose waits give up on the same stream: tt_sync reports the
+    # bit and leaves it; tt_get_error then reads and clears it
+    w = wl.custom("sync_commit", 4, 256, 4, 1, 64, 16, (16,) * 4, V=131072, k=16)
+    ci = wl.commit_inputs(w, seed=1)
+    with torch.cuda.stream(s):
+        c = wl.commit_tensors(ci, "cuda")
+        h.set_wait_timeout(1)
+        try:
+            tt.commit(c["logits"], w.B, w.L, c["masked"], w.k, c["tok"], stream=s)
+            done, st = h.sync(stream=s, timeout_ms=60000)
+        finally:
+            h.set_wait_timeout(DEFAULT_NS)
+    assert done and st & tt.TT_DEV_WAIT_TIMEOUT
+    assert h.get_error() & tt.TT_DEV_WAIT_TIMEOUT
+    assert h.get_error() == 0
+    # and a normal commit on that stream is exact once the stream has drained
+    with torch.cuda.stream(s):
+        c = wl.commit_tensors(ci, "cuda")
+        tok, masked = tt.commit(c["logits"], w.B, w.L, c["masked"], w.k, c["tok"], stream=s)
+    done, st = h.sync(stream=s, timeout_ms=60000)
+    assert done and st == 0
+    ot, om, _, _ = oracle_lib.commit(ci.logits, w.B, w.L, ci.masked, w.k, ci.tok)
+    assert np.array_equal(tok.cpu().numpy(), ot)
+    assert np.array_equal(masked.cpu().numpy(), om)
