@@ -73,6 +73,8 @@ def test_tiny_full_denoise_loop(tt, oracle_lib):
     (2, 1030, 256, 9, 0.8),     # L above the select kernel's 1024 threads
     (2, 24, 100000, 5, 0.8),    # each CTA's quarter ends in a partial 16384-logit chunk
     (1, 16, 131068, 3, 1.0),    # largest V below the limit: the last quarter is ragged
+    (1, 4100, 64, 37, 0.7),     # L above the 2048 staged keys: ranks counted chunk by chunk
+    (2, 16384, 16, 300, 0.5),   # the largest block (16384 rows); V = 16 makes key ties common
 ])
 def test_shapes_and_masks(tt, oracle_lib, case):
     B, L, V, k, frac = case

@@ -51,6 +51,7 @@ def _check(tt, oracle_lib, logits, B, L, masked, gamma, steps_left, tok):
     (2, 300, 4096, 0.9, 5),     # L above the register select (general path)
     (5, 16, 2048, 0.7, 1),      # last step: everything commits
     (1, 1, 4, 1.0, 2),
+    (1, 4100, 64, 0.8, 7),      # L above the 2048 staged keys: ranks counted chunk by chunk
 ])
 @pytest.mark.parametrize("where", ["none", "median", "all"])
 def test_threshold_shapes(tt, oracle_lib, case, where):
