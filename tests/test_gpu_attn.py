@@ -67,6 +67,29 @@ def test_small_cases(tt, oracle_lib, case):
     _assert_close(got, ref)
 
 
+EXTREME = [
+    # the largest query group, Hq/Hkv = 128: one block position per 128-row
+    # query tile, and an odd tile count (a pair with one tile)
+    ("gqa128_max_group", 2, 3, 128, 1, 64, 200, (200, 57), 0.0),
+    # a long block: 9 block KV tiles, the last one partial, and 18 query tiles
+    ("long_block_nine_tiles", 1, 1100, 4, 2, 128, 300, (300,), 0.0),
+]
+
+
+@pytest.mark.parametrize("sched", KERNELS, ids=["per_unit", "persistent"])
+@pytest.mark.parametrize("causal", [False, True], ids=["bidirectional", "causal"])
+@pytest.mark.parametrize("case", EXTREME, ids=[c[0] for c in EXTREME])
+def test_extreme_shapes(tt, oracle_lib, case, causal, sched):
+    name, B, L, Hq, Hkv, D, cap, ctx, qk = case
+    w = wl.custom(name, B, L, Hq, Hkv, D, cap, ctx, qk_std=qk)
+    inp = wl.attn_inputs(w, seed=3)
+    with attn_schedule(tt, *sched):
+        got, _ = _run_gpu(tt, inp, causal=causal)
+    ref = oracle_lib.block_attn(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx, inp.v_ctx, inp.ctx_len,
+                                causal=causal)
+    _assert_close(got, ref)
+
+
 @pytest.mark.parametrize("sched", SCHEDULES)
 def test_schedules_cut_and_merge(tt, oracle_lib, sched):
     # query tiles cut between CTAs at every tile boundary, merged by the last piece
