@@ -90,6 +90,20 @@ def test_extreme_shapes(tt, oracle_lib, case, causal, sched):
     _assert_close(got, ref)
 
 
+@pytest.mark.parametrize("sched", KERNELS, ids=["per_unit", "persistent"])
+def test_two_million_position_context(tt, oracle_lib, sched):
+    # a 2^21-position cache, all but 3 positions filled, behind an 8-token
+    # block: the one-unit-per-CTA schedule splits the one unit 64 ways, the
+    # persistent one cuts its query tile into one piece per SM and merges them
+    # in the kernel
+    w = wl.custom("ctx2m", 1, 8, 4, 1, 64, 1 << 21, ((1 << 21) - 3,))
+    inp = wl.attn_inputs(w, seed=4)
+    with attn_schedule(tt, *sched):
+        got, _ = _run_gpu(tt, inp)
+    ref = oracle_lib.block_attn(inp.q, inp.k_blk, inp.v_blk, inp.k_ctx, inp.v_ctx, inp.ctx_len)
+    _assert_close(got, ref)
+
+
 @pytest.mark.parametrize("sched", SCHEDULES)
 def test_schedules_cut_and_merge(tt, oracle_lib, sched):
     # query tiles cut between CTAs at every tile boundary, merged by the last piece
