@@ -75,6 +75,7 @@ def test_tiny_full_denoise_loop(tt, oracle_lib):
     (1, 16, 131068, 3, 1.0),    # largest V below the limit: the last quarter is ragged
     (1, 4100, 64, 37, 0.7),     # L above the 2048 staged keys: ranks counted chunk by chunk
     (2, 16384, 16, 300, 0.5),   # the largest block (16384 rows); V = 16 makes key ties common
+    (4096, 4, 64, 1, 0.6),      # many small blocks: each cluster's share spans ~100 blocks
 ])
 def test_shapes_and_masks(tt, oracle_lib, case):
     B, L, V, k, frac = case

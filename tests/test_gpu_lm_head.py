@@ -123,7 +123,8 @@ def _commit_pair(tt, oracle_lib, hid, wt, B, L, masked, k, tok, alias, blocks=No
 @pytest.mark.parametrize("alias", [False, True], ids=["separate", "in_place"])
 @pytest.mark.parametrize("B,L,K,V,k,frac", [(4, 32, 256, 4096, 4, 1.0), (3, 50, 136, 1000, 7, 0.6),
                                             (2, 300, 64, 8200, 64, 0.9), (1, 1, 8, 4, 1, 1.0),
-                                            (1, 4100, 8, 64, 37, 0.7), (1, 16384, 8, 64, 300, 0.5)])
+                                            (1, 4100, 8, 64, 37, 0.7), (1, 16384, 8, 64, 300, 0.5),
+                                            (4096, 4, 8, 64, 1, 0.6)])
 def test_commit_behind_the_lm_head(tt, oracle_lib, B, L, K, V, k, frac, alias):
     w = wl.custom("lmc", B, L, 1, 1, 8, 8, (0,) * B, V=V, k=k)
     hid, wt = wl.lm_head_exact_inputs(B * L, K, V, seed=7 + L)
