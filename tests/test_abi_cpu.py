@@ -68,6 +68,19 @@ def test_host_argument_errors(tt):
     assert lib.tt_commit_noalloc(None, 1, 1, 4, None, 0, None, None, None) == -1
 
 
+def test_status_codes_agree_with_the_header(tt):
+    # every tt_status value of the header: the binding's constant of the same
+    # name and the library's name for it
+    src = open(os.path.join(ROOT, "include", "tt.h")).read()
+    codes = dict((n, int(v)) for n, v in re.findall(r"\b(TT_(?:OK|ERR_[A-Z_]+))\s*=\s*(-?\d+)", src))
+    assert codes["TT_OK"] == 0 and len(codes) >= 7
+    for name, value in codes.items():
+        assert getattr(tt, name) == value, name
+        assert tt.lib().tt_status_string(value) == name.encode()
+    bits = dict((n, int(v)) for n, v in re.findall(r"#define\s+(TT_DEV_[A-Z_]+)\s+(\d+)", src))
+    assert bits and all(getattr(tt, n) == v for n, v in bits.items())
+
+
 def test_create_without_gpu_fails_cleanly(tt):
     import torch
     if torch.cuda.is_available():
